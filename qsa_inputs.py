@@ -1,0 +1,175 @@
+"""Seeded synthetic inputs for the QSA block scorer and top-k select.
+
+This module only builds input arrays. It holds none of the method's arithmetic
+(no dot products, no ReLU, no head sums, no ranking), so the CPU oracle and the
+CUDA path can both draw their inputs from it without sharing any computation.
+
+Shapes follow the scorer's statement of the problem (Strata PR #228, part 1,
+"qsa_block_scores_wmma"): q is [nq, H, D] fp16 with D contiguous, kb is one key
+vector per KV block, [nb, D] fp16, and nb = ceil(n_kv / block).
+
+Every array is drawn in float64 from ``numpy.random.default_rng(seed)`` and
+rounded once to fp16 (round to nearest even, numpy ``astype``).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic workload: shapes, selection size and value recipe."""
+
+    name: str
+    nq: int
+    H: int
+    D: int
+    n_kv: int
+    block: int
+    k: int
+    dist: str  # "normal1", "normal_d", "normal_d_x8", "normal_d_onehot"
+    seed: int
+
+    @property
+    def nb(self) -> int:
+        return -(-self.n_kv // self.block)
+
+    @property
+    def n_full(self) -> int:
+        return self.n_kv // self.block
+
+    @property
+    def has_tail(self) -> bool:
+        return self.n_kv % self.block != 0
+
+
+# The five workloads: a tiny CPU-checkable case, short, mid and long (128K)
+# contexts at nq=256, and a large prefill batch with one-hot key rows.
+WORKLOADS = [
+    Workload("tiny_nq16_h4_d64_kv4000", 16, 4, 64, 4000, 64, 8, "normal1", 1001),
+    Workload("short_nq256_h8_d128_kv1024", 256, 8, 128, 1024, 64, 8, "normal_d", 1002),
+    Workload("mid_nq256_h8_d128_kv32805", 256, 8, 128, 32768 + 37, 64, 32, "normal_d", 1003),
+    Workload("long128k_nq256_h8_d128_kv131072", 256, 8, 128, 131072, 64, 64, "normal_d_x8", 1004),
+    Workload("prefill_nq4096_h16_d128_kv131073", 4096, 16, 128, 131072 + 1, 64, 64, "normal_d_onehot", 1005),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def _f16(x: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float16))
+
+
+def make_inputs(w: Workload):
+    """Return (q f16 [nq,H,D], kb f16 [nb,D]) for workload ``w``.
+
+    normal1:          q, kb ~ N(0, 1)
+    normal_d:         q, kb ~ N(0, 1/sqrt(D)) (standard deviation 1/sqrt(D))
+    normal_d_x8:      as normal_d, both multiplied by 8 before rounding
+    normal_d_onehot:  as normal_d; then ceil(1% of nb) kb rows are replaced by
+                      one-hot rows (value 4.0 at a drawn coordinate), and the
+                      second chosen row is forced onto the first one's
+                      coordinate so that exact score ties exist.
+    """
+    rng = np.random.default_rng(w.seed)
+    nb = w.nb
+    if w.dist == "normal1":
+        sd = 1.0
+    else:
+        sd = 1.0 / math.sqrt(w.D)
+    q = rng.normal(0.0, sd, size=(w.nq, w.H, w.D))
+    kb = rng.normal(0.0, sd, size=(nb, w.D))
+    if w.dist == "normal_d_x8":
+        q = q * 8.0
+        kb = kb * 8.0
+    if w.dist == "normal_d_onehot":
+        n_hot = math.ceil(0.01 * nb)
+        rows = rng.choice(nb, size=n_hot, replace=False)
+        coords = rng.integers(0, w.D, size=n_hot)
+        if n_hot >= 2:
+            coords[1] = coords[0]
+        for r, c in zip(rows, coords):
+            kb[r, :] = 0.0
+            kb[r, c] = 4.0
+    return _f16(q), _f16(kb)
+
+
+def make_f32_inputs(w: Workload):
+    """Workload inputs as the f32 arrays that feed the fp32->fp16 stage.
+
+    The f32 values are the drawn float64 values rounded to float32 (not to
+    fp16), so the conversion stage has real rounding work to do.
+    """
+    rng = np.random.default_rng(w.seed + 7919)
+    sd = 1.0 if w.dist == "normal1" else 1.0 / math.sqrt(w.D)
+    scale = 8.0 if w.dist == "normal_d_x8" else 1.0
+    q = rng.normal(0.0, sd, size=(w.nq, w.H, w.D)) * scale
+    kb = rng.normal(0.0, sd, size=(w.nb, w.D)) * scale
+    return (np.ascontiguousarray(q.astype(np.float32)),
+            np.ascontiguousarray(kb.astype(np.float32)))
+
+
+def random_case(nq: int, H: int, D: int, nb: int, seed: int, scale: float = 1.0):
+    """Plain N(0, scale) fp16 q [nq,H,D] and kb [nb,D]."""
+    rng = np.random.default_rng(seed)
+    q = rng.normal(0.0, scale, size=(nq, H, D))
+    kb = rng.normal(0.0, scale, size=(nb, D))
+    return _f16(q), _f16(kb)
+
+
+def coordinate_coded_case(nq: int, H: int, D: int, nb: int):
+    """Coordinate-coded fixture: kb[b] = e_(b mod D) (one-hot, value 1) and
+    q[qi,h,i] = ((7*qi + 3*h + i) mod 61) - 30, small integers exact in fp16.
+
+    Each score then depends on one coordinate of each head only, so a
+    transposed operand, a duplicated lane or a misplaced store changes the
+    value; the expected result is exact at zero tolerance.
+    """
+    qi = np.arange(nq)[:, None, None]
+    h = np.arange(H)[None, :, None]
+    i = np.arange(D)[None, None, :]
+    q = ((7 * qi + 3 * h + i) % 61) - 30
+    kb = np.zeros((nb, D))
+    kb[np.arange(nb), np.arange(nb) % D] = 1.0
+    return _f16(q), _f16(kb)
+
+
+def one_hot_case(nq: int, H: int, D: int, nb: int, seed: int):
+    """One-hot q rows and one-hot kb rows (value 1 at a drawn coordinate)."""
+    rng = np.random.default_rng(seed)
+    q = np.zeros((nq, H, D))
+    cq = rng.integers(0, D, size=(nq, H))
+    for a in range(nq):
+        for b in range(H):
+            q[a, b, cq[a, b]] = 1.0
+    kb = np.zeros((nb, D))
+    ck = rng.integers(0, D, size=nb)
+    kb[np.arange(nb), ck] = 1.0
+    return _f16(q), _f16(kb)
+
+
+def random_scores(nq: int, nb: int, seed: int, kind: str = "normal"):
+    """f32 score matrices for the select stage on its own.
+
+    normal:   N(0,1) f32
+    ties:     small integers, so that many exact ties exist
+    signed0:  a mix of +0.0, -0.0 and a few positive values
+    const:    every entry equal
+    """
+    rng = np.random.default_rng(seed)
+    if kind == "normal":
+        s = rng.normal(0.0, 1.0, size=(nq, nb))
+    elif kind == "ties":
+        s = rng.integers(-3, 4, size=(nq, nb)).astype(np.float64)
+    elif kind == "signed0":
+        s = np.where(rng.random((nq, nb)) < 0.5, 0.0, -0.0)
+        hot = rng.random((nq, nb)) < 0.05
+        s = np.where(hot, rng.random((nq, nb)) + 0.5, s)
+    elif kind == "const":
+        s = np.full((nq, nb), 1.25)
+    else:
+        raise ValueError(kind)
+    return np.ascontiguousarray(s.astype(np.float32))
