@@ -1,0 +1,181 @@
+/*
+ * qsa.h - C ABI of libqsa, a GB300 (sm_103a) library for QSA block scoring and
+ * top-k block selection.
+ *
+ * The operation (Strata pull request 228, part 1, "qsa_block_scores_wmma: the
+ * prompt scorer arm on tensor cores"): for every query qi and KV block b,
+ *
+ *     score(qi, b) = sum_{h < H} relu( sum_{i < D} kb[b, i] * q[qi, h, i] )
+ *
+ * with fp16 operands and fp32 accumulation, followed by the selection of the k
+ * highest-scoring blocks per query. A context of n_kv tokens is cut into
+ * nb = ceil(n_kv / block) blocks; when n_kv % block != 0 the last block is a
+ * partial "tail" that a separate kernel scores in one fixed fp32 order and
+ * forces into the selection by adding 1e9 to its score (Strata pull request
+ * 856, section "What": the shared tail-block kernel and the +1e9 dead-tail
+ * rule).
+ *
+ * Conventions for every entry point:
+ *   - Buffers are device pointers owned by the caller unless stated otherwise.
+ *     The library allocates no device memory and keeps no pointer after a
+ *     call returns.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and runs asynchronously; no entry point synchronizes except
+ *     qsa_device_status().
+ *   - Arguments are validated on the host before anything is launched. A
+ *     failed check returns an error status and launches nothing. There is no
+ *     CPU fallback: every result is computed by the library's CUDA kernels.
+ *   - Empty work (nq == 0, nb == 0, n == 0) returns QSA_OK without a launch.
+ *   - The device must be compute capability 10.3 (sm_103a); other devices get
+ *     QSA_ERR_UNSUPPORTED_ARCH.
+ *   - Kernels bound every wait; a wait that runs out records a timeout in a
+ *     device status word that qsa_device_status() reports.
+ *   - Not thread-safe per stream in the sense of CUDA streams only: calls from
+ *     several host threads are safe; work on one stream runs in order.
+ */
+#ifndef QSA_H_
+#define QSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without CUDA headers. */
+typedef struct CUstream_st* qsa_stream_t;
+
+typedef enum {
+  QSA_OK = 0,
+  QSA_ERR_INVALID_ARG = 1,          /* null pointer, negative size, k < 1, block < 1 ... */
+  QSA_ERR_UNSUPPORTED_GEOMETRY = 2, /* H, D, k or nb outside the supported ranges below */
+  QSA_ERR_UNSUPPORTED_ARCH = 3,     /* current device is not sm_103 */
+  QSA_ERR_MISALIGNED = 4,           /* a pointer breaks the alignment rule stated below */
+  QSA_ERR_CUDA = 5,                 /* a CUDA runtime/driver call or launch failed */
+  QSA_ERR_TIMEOUT = 6               /* a kernel gave up a bounded wait (qsa_device_status) */
+} qsa_status;
+
+/* ABI version of this header; bumps when a signature changes. */
+#define QSA_ABI_VERSION 1
+int qsa_abi_version(void);
+
+/* Static, NUL-terminated name of a status code. */
+const char* qsa_status_str(qsa_status status);
+
+/* Static, NUL-terminated description of the kernels that run (the "arm"),
+ * so that no other path can pass for this one (after Strata pull request 228,
+ * part 1, which prints the arm that ran). */
+const char* qsa_arm(void);
+
+/* nb = ceil(n_kv / block): the number of KV blocks, the tail included.
+ * Returns -1 if n_kv < 0 or block < 1. */
+int64_t qsa_num_blocks(int64_t n_kv, int32_t block);
+
+/*
+ * qsa_f32_to_f16 - the FP32 -> FP16 operand conversion stage (Strata pull
+ * request 228, part 1: f32_to_f16_poison_kernel runs beside the scorer; the
+ * "fp16 conversion" is part of the qsa select phase).
+ *
+ *   src  f32[n], dst f16[n] (raw binary16 bits, uint16_t), device memory.
+ *   dst[i] = binary16 round-to-nearest-even of src[i]; overflow gives +-inf;
+ *   NaN gives a NaN (its payload is not kept).
+ *   src and dst must not overlap. Any alignment of 4 (src) / 2 (dst) bytes
+ *   works; 16-byte aligned buffers take the vectorised path.
+ *   Errors: QSA_ERR_INVALID_ARG for n < 0 or a null pointer with n > 0;
+ *   QSA_ERR_MISALIGNED for a src not 4-byte or dst not 2-byte aligned.
+ */
+qsa_status qsa_f32_to_f16(const float* src, uint16_t* dst, int64_t n, qsa_stream_t stream);
+
+/*
+ * qsa_block_scores - every block score, tail included (Strata pull request
+ * 228, part 1, the score definition; pull request 856, "What", the tail).
+ *
+ *   q       f16 [nq, H, D] row-major (D contiguous), device, 16-byte aligned.
+ *   kb      f16 [nb, D] row-major, one key vector per block, device, 16-byte
+ *           aligned; must hold nb = ceil(n_kv / block) rows (the C ABI cannot
+ *           check this, the Python binding does).
+ *   scores  f32 [nq, nb] row-major, device, 16-byte aligned; written exactly
+ *           once per entry and nowhere else.
+ *   Full blocks b < n_kv / block: fp16 x fp16 products accumulated in fp32 by
+ *   the tensor cores (tcgen05), then per-head ReLU and the head sum in fp32.
+ *   Each such score lies within B = 2^-9.5 * S + 8 * 2^-24 * |score| of the
+ *   exact score, S = sum over h and i of |q * kb|.
+ *   Tail block (n_kv % block != 0, column nb-1): acc_h = sequential fp32 sum
+ *   over i of q[qi,h,i]*kb[nb-1,i]; t = sequential fp32 sum over h of
+ *   max(acc_h, 0); score = t + 1e9f, each step rounded to nearest even.
+ *   Supported: nq >= 0; H in {1, 2, 4, 8, 16, 32}; D a multiple of 16 with
+ *   16 <= D <= 256; block >= 1; n_kv >= 0; nq * H < 2^31; nb < 2^31.
+ *   Inputs must be finite.
+ */
+qsa_status qsa_block_scores(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H,
+                            int32_t D, int64_t n_kv, int32_t block, float* scores,
+                            qsa_stream_t stream);
+
+/*
+ * qsa_select - top-k block selection per query (Strata pull request 228,
+ * part 1; pull request 856, "Arithmetic contract and parity": top-k over the
+ * block scores).
+ *
+ *   scores  f32 [nq, nb] row-major, device, 4-byte aligned, finite (NaN is
+ *           not supported).
+ *   ids     int32 [nq, k] row-major, device, 4-byte aligned.
+ *   ids[qi, :] lists the min(k, nb) blocks with the largest scores, in
+ *   descending score order; equal scores are ordered by ascending block index
+ *   (the smaller index wins a tie at the k-th place); -0.0 and +0.0 are
+ *   equal; entries past nb (when nb < k) are -1. Exact: no tolerance.
+ *   Supported: 1 <= k <= 1024; 0 <= nb <= 32768.
+ */
+qsa_status qsa_select(const float* scores, int32_t nq, int32_t nb, int32_t k, int32_t* ids,
+                      qsa_stream_t stream);
+
+/*
+ * qsa_score_select - the metric path: qsa_block_scores followed by qsa_select
+ * on the same stream, with the same arguments and rules as those two. Both
+ * outputs are written: scores [nq, nb] and ids [nq, k].
+ */
+qsa_status qsa_score_select(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H,
+                            int32_t D, int64_t n_kv, int32_t block, int32_t k, float* scores,
+                            int32_t* ids, qsa_stream_t stream);
+
+/*
+ * qsa_select_step - one whole pass of the selection phase for one query
+ * batch: q arrives as f32, is converted to fp16 into the caller's q16 buffer
+ * (qsa_f32_to_f16), then scored and selected (qsa_score_select).
+ *
+ *   q32  f32 [nq, H, D] device; q16 f16 [nq, H, D] device, 16-byte aligned,
+ *   written by the call; the other arguments as for qsa_score_select.
+ */
+qsa_status qsa_select_step(const float* q32, uint16_t* q16, const uint16_t* kb, int32_t nq,
+                           int32_t H, int32_t D, int64_t n_kv, int32_t block, int32_t k,
+                           float* scores, int32_t* ids, qsa_stream_t stream);
+
+/*
+ * qsa_select_step_host - qsa_select_step from HOST buffers: enqueues on
+ * `stream` the copies q32_host -> q32_dev and kb_host -> kb_dev, the step,
+ * and the copies scores_dev -> scores_host and ids_dev -> ids_host. Host
+ * buffers should be page-locked for the copies to be asynchronous; they must
+ * stay valid until the stream has finished the call's work (synchronize the
+ * stream before reading scores_host / ids_host). Device buffers are the
+ * caller's, sized as for qsa_select_step (kb_dev: nb rows).
+ */
+qsa_status qsa_select_step_host(const float* q32_host, const uint16_t* kb_host, int32_t nq,
+                                int32_t H, int32_t D, int64_t n_kv, int32_t block, int32_t k,
+                                float* scores_host, int32_t* ids_host, float* q32_dev,
+                                uint16_t* q16_dev, uint16_t* kb_dev, float* scores_dev,
+                                int32_t* ids_dev, qsa_stream_t stream);
+
+/*
+ * qsa_device_status - synchronizes `stream`, then reads the current device's
+ * status word, where kernels record a bounded wait that ran out. Returns
+ * QSA_OK if it is clear, QSA_ERR_TIMEOUT if not (and clears it when `clear`
+ * is nonzero), or QSA_ERR_CUDA if the synchronization itself failed. The
+ * word's raw bits are stored in *bits when bits is not NULL.
+ */
+qsa_status qsa_device_status(int clear, uint32_t* bits, qsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H_ */

@@ -1,0 +1,240 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Scores of full blocks must lie within the pages' bound B of the float64
+oracle; the tail column must equal the oracle's fp32 tail bit for bit; the
+select must equal the oracle's top-k of the same GPU scores bit for bit, and
+agree with the oracle's top-k of the exact scores except where the k-th /
+(k+1)-th gap is below 2B; the fp16 conversion must be bitwise.
+"""
+import numpy as np
+import pytest
+
+import qsa_inputs as qi
+from oracle import qsa_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def tbs():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from top_block_selection_gb300 import _build
+    _build.build()
+    import top_block_selection_gb300 as m
+    m.load_library()
+    return m
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+UTIL = {}
+
+
+def check_case(tbs, q, kb, n_kv, block, k, name, exact=False):
+    s_gpu, ids_gpu = tbs.qsa_score_select(dev(q), dev(kb), n_kv, k, block)
+    torch.cuda.synchronize()
+    s = s_gpu.cpu().numpy()
+    ids = ids_gpu.cpu().numpy()
+    s_ref, S, B, tail = orc.reference_scores(q, kb, n_kv, block)
+    assert s.shape == s_ref.shape and s.dtype == np.float32
+    if exact:
+        assert np.array_equal(s.astype(np.float64), s_ref), name
+    rep = orc.bound_report(s, s_ref, B)
+    assert rep["ok"], (name, rep)
+    UTIL[name] = rep["worst_util"]
+    if tail is not None:
+        assert s[:, -1].view(np.uint32).tolist() == tail.view(np.uint32).tolist(), name
+    # exact select of the GPU's own scores
+    assert np.array_equal(ids, orc.select_topk(s, k)), name
+    sel = orc.selection_report(ids, s_ref, B, k)
+    assert sel["ok"], (name, sel)
+    return rep, sel
+
+
+@pytest.mark.parametrize("w", qi.WORKLOADS, ids=[w.name for w in qi.WORKLOADS])
+def test_workload_parity(tbs, w):
+    q, kb = qi.make_inputs(w)
+    rep, sel = check_case(tbs, q, kb, w.n_kv, w.block, w.k, w.name)
+    print(f"{w.name}: worst bound utilisation {rep['worst_util']:.4f}, "
+          f"guarded rows {sel['guarded_rows']}, exact rows {sel['exact_rows']}")
+
+
+@pytest.mark.parametrize("H", [1, 2, 4, 8, 16, 32])
+@pytest.mark.parametrize("D", [16, 64, 80, 128, 256])
+def test_coordinate_coded_exact(tbs, H, D):
+    nq, nb, block = 19, 300, 16
+    q, kb = qi.coordinate_coded_case(nq, H, D, nb)
+    check_case(tbs, q, kb, nb * block - 5, block, 7, f"coord-H{H}-D{D}", exact=True)
+
+
+def test_one_hot_exact(tbs):
+    q, kb = qi.one_hot_case(40, 8, 128, 260, seed=11)
+    check_case(tbs, q, kb, 260 * 64, 64, 16, "one-hot", exact=True)
+
+
+@pytest.mark.parametrize("nq", [1, 17, 129])
+@pytest.mark.parametrize("nb,tail", [(1, False), (1, True), (63, True), (129, False), (129, True)])
+def test_ragged_tiles(tbs, nq, nb, tail):
+    block = 64
+    n_kv = nb * block - (13 if tail else 0)
+    q, kb = qi.random_case(nq, 8, 128, nb, seed=nq * 1000 + nb, scale=0.3)
+    check_case(tbs, q, kb, n_kv, block, 8, f"ragged-{nq}-{nb}-{tail}")
+
+
+@pytest.mark.parametrize("H,D", [(1, 64), (2, 256), (4, 48), (16, 128), (32, 32)])
+def test_other_geometries(tbs, H, D):
+    nq, nb = 45, 700
+    q, kb = qi.random_case(nq, H, D, nb, seed=H * 7 + D, scale=0.5)
+    check_case(tbs, q, kb, nb * 64 - 1, 64, 24, f"geom-H{H}-D{D}")
+
+
+def test_x8_headroom(tbs):
+    q, kb = qi.random_case(64, 8, 128, 200, seed=5, scale=8.0 / np.sqrt(128) * 4)
+    check_case(tbs, q, kb, 200 * 64, 64, 32, "x8-headroom")
+
+
+def test_empty_and_degenerate(tbs):
+    q, kb = qi.random_case(5, 8, 128, 10, seed=1)
+    s, ids = tbs.qsa_score_select(dev(q), dev(kb), 0, 4, 64)
+    torch.cuda.synchronize()
+    assert tuple(s.shape) == (5, 0) and ids.cpu().numpy().tolist() == [[-1] * 4] * 5
+    # n_kv < block: only the tail block
+    check_case(tbs, q, kb, 10, 64, 4, "tail-only")
+    # nq == 0
+    s, ids = tbs.qsa_score_select(dev(q[:0]), dev(kb), 640, 4, 64)
+    assert tuple(s.shape) == (0, 10) and tuple(ids.shape) == (0, 4)
+
+
+def test_write_set_canaries(tbs):
+    nq, H, D, nb, k, block = 33, 8, 128, 150, 10, 64
+    q, kb = qi.random_case(nq, H, D, nb, seed=77)
+    n_kv = nb * block - 3
+    guard = 64
+    sbuf = torch.full((guard + nq * nb + guard,), float("nan"), dtype=torch.float32, device="cuda")
+    sbuf.view(torch.int32).fill_(0x7FC0DEAD)
+    ibuf = torch.full((guard + nq * k + guard,), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    s_view = sbuf[guard:guard + nq * nb].view(nq, nb)
+    i_view = ibuf[guard:guard + nq * k].view(nq, k)
+    tbs.qsa_score_select(dev(q), dev(kb), n_kv, k, block, scores=s_view, ids=i_view)
+    torch.cuda.synchronize()
+    sb = sbuf.view(torch.int32).cpu().numpy()
+    ib = ibuf.cpu().numpy()
+    assert np.all(sb[:guard] == 0x7FC0DEAD) and np.all(sb[-guard:] == 0x7FC0DEAD)
+    assert np.all(ib[:guard] == 0x5A5A5A5A) and np.all(ib[-guard:] == 0x5A5A5A5A)
+    assert not np.any(sb[guard:-guard] == 0x7FC0DEAD)       # every entry written
+    assert not np.any(ib[guard:-guard] == 0x5A5A5A5A)
+
+
+def test_determinism_double_launch(tbs):
+    w = qi.WORKLOADS[3]
+    q, kb = qi.make_inputs(w)
+    qd, kd = dev(q), dev(kb)
+    s1, i1 = tbs.qsa_score_select(qd, kd, w.n_kv, w.k, w.block)
+    s2, i2 = tbs.qsa_score_select(qd, kd, w.n_kv, w.k, w.block)
+    torch.cuda.synchronize()
+    assert torch.equal(s1.view(torch.int32), s2.view(torch.int32))
+    assert torch.equal(i1, i2)
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties", "signed0", "const"])
+@pytest.mark.parametrize("nb,k", [(1, 1), (5, 8), (33, 8), (100, 64), (1000, 100), (2049, 64),
+                                  (4096, 1024), (32768, 64), (300, 300)])
+def test_select_exact(tbs, kind, nb, k):
+    nq = 3 if nb >= 4096 else 23
+    s = qi.random_scores(nq, nb, seed=nb * 31 + k, kind=kind)
+    ids = tbs.qsa_select(dev(s), k)
+    torch.cuda.synchronize()
+    assert np.array_equal(ids.cpu().numpy(), orc.select_topk(s, k))
+
+
+def test_select_empty_rows(tbs):
+    ids = tbs.qsa_select(torch.zeros((4, 0), dtype=torch.float32, device="cuda"), 3)
+    torch.cuda.synchronize()
+    assert ids.cpu().numpy().tolist() == [[-1] * 3] * 4
+
+
+def test_convert_bitwise(tbs):
+    rng = np.random.default_rng(3)
+    vals = np.concatenate([
+        np.array([0.0, -0.0, 65504.0, 65519.99, 65520.0, -65520.0, 1e6, 2.0 ** -24, 2.0 ** -25,
+                  3 * 2.0 ** -26, 2.0 ** -14, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, np.inf, -np.inf]),
+        rng.normal(size=100003) * np.exp2(rng.integers(-30, 17, size=100003))]).astype(np.float32)
+    out = tbs.qsa_f32_to_f16(dev(vals)).cpu().numpy()
+    assert np.array_equal(out.view(np.uint16), orc.f32_to_f16(vals).view(np.uint16))
+    # an unaligned view takes the scalar path
+    x = dev(vals)[1:]
+    out2 = tbs.qsa_f32_to_f16(x.contiguous())
+    assert np.array_equal(out2.cpu().numpy().view(np.uint16), orc.f32_to_f16(vals[1:]).view(np.uint16))
+    nan = tbs.qsa_f32_to_f16(dev(np.array([np.nan] * 9, np.float32))).cpu().numpy()
+    assert np.all(np.isnan(nan))
+
+
+@pytest.mark.parametrize("w", qi.WORKLOADS[:4], ids=[w.name for w in qi.WORKLOADS[:4]])
+def test_select_step_from_f32(tbs, w):
+    """Start from f32 queries and keys: the conversion runs on the GPU and the
+    scores are compared with the float64 oracle on the f32 ORIGINALS, which
+    exercises the 2^-9.5 * S operand-rounding term of the bound."""
+    q32, kb32 = qi.make_f32_inputs(w)
+    kb16_gpu = tbs.qsa_f32_to_f16(dev(kb32))
+    q16_gpu, s_gpu, ids_gpu = tbs.qsa_select_step(dev(q32), kb16_gpu, w.n_kv, w.k, w.block)
+    torch.cuda.synchronize()
+    kb16 = orc.f32_to_f16(kb32)
+    assert np.array_equal(kb16_gpu.cpu().numpy().view(np.uint16), kb16.view(np.uint16))
+    q16 = q16_gpu.cpu().numpy()
+    assert np.array_equal(q16.view(np.uint16), orc.f32_to_f16(q32).view(np.uint16))
+    s = s_gpu.cpu().numpy()
+    s_ref32 = orc.scores_f64(q32.astype(np.float64), kb32.astype(np.float64), w.n_kv, w.block)
+    S32 = orc.abs_product_sum_f64(q32.astype(np.float64), kb32.astype(np.float64), w.n_kv, w.block)
+    B32 = orc.error_bound(S32, s_ref32)
+    full = slice(0, w.n_full)
+    rep = orc.bound_report(s[:, full], s_ref32[:, full], B32[:, full])
+    assert rep["ok"], rep
+    UTIL[w.name + "-f32"] = rep["worst_util"]
+    tail = orc.tail_scores_f32(q16, kb16, w.n_kv, w.block)
+    if tail is not None:
+        assert s[:, -1].view(np.uint32).tolist() == tail.view(np.uint32).tolist()
+    assert np.array_equal(ids_gpu.cpu().numpy(), orc.select_topk(s, w.k))
+
+
+def test_select_step_host_matches_device(tbs):
+    w = qi.WORKLOADS[2]
+    q32, kb16 = qi.make_f32_inputs(w)[0], qi.make_inputs(w)[1]
+    q32h = torch.from_numpy(q32).pin_memory()
+    kbh = torch.from_numpy(kb16).pin_memory()
+    sh = torch.empty((w.nq, w.nb), dtype=torch.float32).pin_memory()
+    ih = torch.empty((w.nq, w.k), dtype=torch.int32).pin_memory()
+    bufs = (torch.empty_like(q32h, device="cuda"), torch.empty(q32.shape, dtype=torch.float16, device="cuda"),
+            torch.empty_like(kbh, device="cuda"), torch.empty_like(sh, device="cuda"),
+            torch.empty_like(ih, device="cuda"))
+    tbs.qsa_select_step_host(q32h, kbh, w.n_kv, w.k, w.block, sh, ih, bufs)
+    torch.cuda.synchronize()
+    _, s_d, i_d = tbs.qsa_select_step(dev(q32), dev(kb16), w.n_kv, w.k, w.block)
+    torch.cuda.synchronize()
+    assert np.array_equal(sh.numpy().view(np.uint32), s_d.cpu().numpy().view(np.uint32))
+    assert np.array_equal(ih.numpy(), i_d.cpu().numpy())
+
+
+def test_negative_control_on_gpu_scores(tbs):
+    w = qi.WORKLOADS[0]
+    q, kb = qi.make_inputs(w)
+    s = tbs.qsa_block_scores(dev(q), dev(kb), w.n_kv, w.block).cpu().numpy()
+    s_ref, S, B, _ = orc.reference_scores(q, kb, w.n_kv, w.block)
+    assert orc.bound_report(s, s_ref, B)["ok"]
+    bad = s.astype(np.float64) + 2.5 * B
+    assert not orc.bound_report(bad, s_ref, B)["ok"]
+
+
+def test_device_status_clear(tbs):
+    st, bits = tbs.qsa_device_status(clear=True)
+    assert st == 0 and bits == 0
+
+
+def test_report_bound_utilisation():
+    if UTIL:
+        worst = max(UTIL.values())
+        print("worst bound utilisation over GPU cases: %.4f (%s)" % (worst, max(UTIL, key=UTIL.get)))
+        assert worst <= 1.0

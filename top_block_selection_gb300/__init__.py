@@ -1,0 +1,272 @@
+"""Python binding of libqsa: QSA block scores and top-k block selection on
+GB300 (sm_103a).
+
+Argument marshalling only: every function checks dtypes, devices, shapes and
+contiguity, allocates outputs with PyTorch when none are given, and calls the
+C entry point of the same name (include/qsa.h) on the current CUDA stream.
+All computation runs in the library's CUDA kernels; there is no other path.
+If libqsa.so is missing or cannot load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "QsaError", "load_library", "library_path", "qsa_abi_version", "qsa_status_str", "qsa_arm",
+    "qsa_num_blocks", "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select",
+    "qsa_select_step", "qsa_select_step_host", "qsa_device_status", "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+# Every symbol declared in include/qsa.h.
+EXPORTED_SYMBOLS = (
+    "qsa_abi_version", "qsa_status_str", "qsa_arm", "qsa_num_blocks", "qsa_f32_to_f16",
+    "qsa_block_scores", "qsa_select", "qsa_score_select", "qsa_select_step",
+    "qsa_select_step_host", "qsa_device_status",
+)
+
+STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED_GEOMETRY",
+                3: "QSA_ERR_UNSUPPORTED_ARCH", 4: "QSA_ERR_MISALIGNED", 5: "QSA_ERR_CUDA",
+                6: "QSA_ERR_TIMEOUT"}
+
+
+class QsaError(RuntimeError):
+    """A libqsa entry point returned a status other than QSA_OK."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+def library_path() -> str:
+    return os.environ.get("QSA_LIBRARY", os.path.join(_HERE, "lib", "libqsa.so"))
+
+
+def load_library():
+    """Load libqsa.so once and declare the C signatures."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libqsa.so not found at {path}: build it with "
+                           "`python -m top_block_selection_gb300._build`")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, u32p = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.POINTER(ctypes.c_uint32)
+    sig = {
+        "qsa_abi_version": (ctypes.c_int, []),
+        "qsa_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+        "qsa_arm": (ctypes.c_char_p, []),
+        "qsa_num_blocks": (i64, [i64, i32]),
+        "qsa_f32_to_f16": (ctypes.c_int, [vp, vp, i64, vp]),
+        "qsa_block_scores": (ctypes.c_int, [vp, vp, i32, i32, i32, i64, i32, vp, vp]),
+        "qsa_select": (ctypes.c_int, [vp, i32, i32, i32, vp, vp]),
+        "qsa_score_select": (ctypes.c_int, [vp, vp, i32, i32, i32, i64, i32, i32, vp, vp, vp]),
+        "qsa_select_step": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i64, i32, i32, vp, vp, vp]),
+        "qsa_select_step_host": (ctypes.c_int, [vp, vp, i32, i32, i32, i64, i32, i32, vp, vp,
+                                                vp, vp, vp, vp, vp, vp]),
+        "qsa_device_status": (ctypes.c_int, [ctypes.c_int, u32p, vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+# ------------------------------------------------------------------ helpers
+def _check(status: int, where: str):
+    if status != 0:
+        raise QsaError(status, where)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_of(t):
+    torch = _torch()
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _need(t, dtype, ndim, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype or t.dim() != ndim or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D CUDA {dtype} tensor, got "
+                         f"{t.dtype} {tuple(t.shape)} on {t.device}")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr() if t.numel() else 0)
+
+
+# -------------------------------------------------------------- entry points
+def qsa_abi_version() -> int:
+    return load_library().qsa_abi_version()
+
+
+def qsa_status_str(status: int) -> str:
+    return load_library().qsa_status_str(status).decode()
+
+
+def qsa_arm() -> str:
+    return load_library().qsa_arm().decode()
+
+
+def qsa_num_blocks(n_kv: int, block: int = 64) -> int:
+    return int(load_library().qsa_num_blocks(n_kv, block))
+
+
+def qsa_f32_to_f16(x, out=None):
+    """fp32 -> fp16 (round to nearest even) of a CUDA float32 tensor."""
+    torch = _torch()
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA float32 tensor")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float16, device=x.device)
+    elif out.shape != x.shape or out.dtype != torch.float16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float16 tensor shaped like x")
+    lib = load_library()
+    with torch.cuda.device(x.device):
+        _check(lib.qsa_f32_to_f16(_ptr(x), _ptr(out), x.numel(), _stream_of(x)), "qsa_f32_to_f16")
+    return out
+
+
+def _score_args(q, kb, n_kv, block):
+    torch = _torch()
+    _need(q, torch.float16, 3, "q")
+    _need(kb, torch.float16, 2, "kb")
+    nq, H, D = q.shape
+    if kb.shape[1] != D:
+        raise ValueError(f"kb has D={kb.shape[1]}, q has D={D}")
+    nb = qsa_num_blocks(n_kv, block)
+    if nb < 0:
+        raise ValueError("n_kv must be >= 0 and block >= 1")
+    if kb.shape[0] < nb:
+        raise ValueError(f"kb must hold nb={nb} rows, has {kb.shape[0]}")
+    if kb.device != q.device:
+        raise ValueError("q and kb must be on the same device")
+    return nq, H, D, nb
+
+
+def qsa_block_scores(q, kb, n_kv: int, block: int = 64, out=None):
+    """scores f32 [nq, nb]: full blocks on the tensor cores, the tail block
+    (if any) by the fp32 tail kernel with the +1e9 bonus."""
+    torch = _torch()
+    nq, H, D, nb = _score_args(q, kb, n_kv, block)
+    if out is None:
+        out = torch.empty((nq, nb), dtype=torch.float32, device=q.device)
+    else:
+        _need(out, torch.float32, 2, "out")
+        if tuple(out.shape) != (nq, nb):
+            raise ValueError(f"out must be [{nq}, {nb}]")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        _check(lib.qsa_block_scores(_ptr(q), _ptr(kb), nq, H, D, n_kv, block, _ptr(out),
+                                    _stream_of(q)), "qsa_block_scores")
+    return out
+
+
+def qsa_select(scores, k: int, out=None):
+    """ids int32 [nq, k]: top-k blocks per row, descending score, smaller index
+    first on ties, -1 padding when nb < k."""
+    torch = _torch()
+    _need(scores, torch.float32, 2, "scores")
+    nq, nb = scores.shape
+    if out is None:
+        out = torch.empty((nq, k), dtype=torch.int32, device=scores.device)
+    else:
+        _need(out, torch.int32, 2, "out")
+        if tuple(out.shape) != (nq, k):
+            raise ValueError(f"out must be [{nq}, {k}]")
+    lib = load_library()
+    with torch.cuda.device(scores.device):
+        _check(lib.qsa_select(_ptr(scores), nq, nb, k, _ptr(out), _stream_of(scores)), "qsa_select")
+    return out
+
+
+def qsa_score_select(q, kb, n_kv: int, k: int, block: int = 64, scores=None, ids=None):
+    """(scores [nq, nb] f32, ids [nq, k] int32) in one call."""
+    torch = _torch()
+    nq, H, D, nb = _score_args(q, kb, n_kv, block)
+    if scores is None:
+        scores = torch.empty((nq, nb), dtype=torch.float32, device=q.device)
+    if ids is None:
+        ids = torch.empty((nq, k), dtype=torch.int32, device=q.device)
+    _need(scores, torch.float32, 2, "scores")
+    _need(ids, torch.int32, 2, "ids")
+    if tuple(scores.shape) != (nq, nb) or tuple(ids.shape) != (nq, k):
+        raise ValueError("scores must be [nq, nb] and ids [nq, k]")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        _check(lib.qsa_score_select(_ptr(q), _ptr(kb), nq, H, D, n_kv, block, k, _ptr(scores),
+                                    _ptr(ids), _stream_of(q)), "qsa_score_select")
+    return scores, ids
+
+
+def qsa_select_step(q32, kb, n_kv: int, k: int, block: int = 64, q16=None, scores=None, ids=None):
+    """One selection step from f32 queries: convert, score, select.
+    Returns (q16, scores, ids)."""
+    torch = _torch()
+    _need(q32, torch.float32, 3, "q32")
+    _need(kb, torch.float16, 2, "kb")
+    nq, H, D = q32.shape
+    nb = qsa_num_blocks(n_kv, block)
+    if nb < 0 or kb.shape[1] != D or kb.shape[0] < nb:
+        raise ValueError("kb must be [>= nb, D] and n_kv >= 0, block >= 1")
+    if q16 is None:
+        q16 = torch.empty((nq, H, D), dtype=torch.float16, device=q32.device)
+    if scores is None:
+        scores = torch.empty((nq, nb), dtype=torch.float32, device=q32.device)
+    if ids is None:
+        ids = torch.empty((nq, k), dtype=torch.int32, device=q32.device)
+    _need(q16, torch.float16, 3, "q16")
+    _need(scores, torch.float32, 2, "scores")
+    _need(ids, torch.int32, 2, "ids")
+    lib = load_library()
+    with torch.cuda.device(q32.device):
+        _check(lib.qsa_select_step(_ptr(q32), _ptr(q16), _ptr(kb), nq, H, D, n_kv, block, k,
+                                   _ptr(scores), _ptr(ids), _stream_of(q32)), "qsa_select_step")
+    return q16, scores, ids
+
+
+def qsa_select_step_host(q32_host, kb_host, n_kv: int, k: int, block: int, scores_host, ids_host,
+                         dev_buffers, stream=None):
+    """qsa_select_step from host (CPU, ideally pinned) tensors. dev_buffers =
+    (q32_dev, q16_dev, kb_dev, scores_dev, ids_dev) CUDA tensors. Enqueued on
+    `stream` (default: current stream); synchronize before reading outputs."""
+    torch = _torch()
+    q32_dev, q16_dev, kb_dev, scores_dev, ids_dev = dev_buffers
+    for t, name in ((q32_host, "q32_host"), (kb_host, "kb_host"), (scores_host, "scores_host"),
+                    (ids_host, "ids_host")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    nq, H, D = q32_host.shape
+    if stream is None:
+        stream = torch.cuda.current_stream(q32_dev.device)
+    lib = load_library()
+    with torch.cuda.device(q32_dev.device):
+        _check(lib.qsa_select_step_host(
+            _ptr(q32_host), _ptr(kb_host), nq, H, D, n_kv, block, k, _ptr(scores_host),
+            _ptr(ids_host), _ptr(q32_dev), _ptr(q16_dev), _ptr(kb_dev), _ptr(scores_dev),
+            _ptr(ids_dev), ctypes.c_void_p(stream.cuda_stream)), "qsa_select_step_host")
+
+
+def qsa_device_status(clear: bool = True, device=None):
+    """Synchronize the current stream and return (status, bits) of the device
+    status word (nonzero bits = a kernel gave up a bounded wait)."""
+    torch = _torch()
+    lib = load_library()
+    bits = ctypes.c_uint32(0)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        st = lib.qsa_device_status(1 if clear else 0, ctypes.byref(bits),
+                                   ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+    return st, bits.value

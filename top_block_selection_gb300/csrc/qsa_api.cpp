@@ -1,0 +1,232 @@
+// qsa_api.cpp - the C ABI (include/qsa.h): host-side validation, block
+// partition, and stream-ordered launches. Arguments are checked before any
+// CUDA call, so a bad call returns a status without touching the device.
+#include "../../include/qsa.h"
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "qsa_internal.h"
+
+namespace {
+
+using qsa::DeviceInfo;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_heads(int32_t H) {
+  return H == 1 || H == 2 || H == 4 || H == 8 || H == 16 || H == 32;
+}
+
+cudaStream_t as_cuda(qsa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Returns the current device's info, or an error status.
+qsa_status device_or_error(const DeviceInfo** out) {
+  cudaError_t e = cudaSuccess;
+  const DeviceInfo* d = qsa::current_device(&e);
+  if (!d) return QSA_ERR_CUDA;
+  if (!d->supported) return QSA_ERR_UNSUPPORTED_ARCH;
+  *out = d;
+  return QSA_OK;
+}
+
+struct Geometry {
+  int64_t nb = 0, n_full = 0;
+  bool has_tail = false;
+};
+
+// Checks shared by every scoring entry point; fills g on success.
+qsa_status check_scores(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H, int32_t D,
+                        int64_t n_kv, int32_t block, const float* scores, Geometry* g) {
+  if (nq < 0 || n_kv < 0 || block < 1 || H < 1 || D < 1) return QSA_ERR_INVALID_ARG;
+  if (!supported_heads(H) || D % 16 != 0 || D < 16 || D > 256) return QSA_ERR_UNSUPPORTED_GEOMETRY;
+  g->nb = n_kv / block + (n_kv % block != 0 ? 1 : 0);
+  g->n_full = n_kv / block;
+  g->has_tail = (n_kv % block) != 0;
+  if (g->nb > 0x7FFFFFFFLL || static_cast<int64_t>(nq) * H > 0x7FFFFFFFLL)
+    return QSA_ERR_UNSUPPORTED_GEOMETRY;
+  if (nq == 0 || g->nb == 0) return QSA_OK;
+  if (!q || !kb || !scores) return QSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kb, 16) || !aligned(scores, 16)) return QSA_ERR_MISALIGNED;
+  return QSA_OK;
+}
+
+qsa_status check_select(const float* scores, int32_t nq, int64_t nb, int32_t k,
+                        const int32_t* ids) {
+  if (nq < 0 || nb < 0 || k < 1) return QSA_ERR_INVALID_ARG;
+  if (k > qsa::kMaxSelectK || nb > qsa::kMaxSelectNb) return QSA_ERR_UNSUPPORTED_GEOMETRY;
+  if (nq == 0) return QSA_OK;
+  if (!ids || (nb > 0 && !scores)) return QSA_ERR_INVALID_ARG;
+  if (!aligned(ids, 4) || !aligned(scores, 4)) return QSA_ERR_MISALIGNED;
+  return QSA_OK;
+}
+
+qsa_status run_scores(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H, int32_t D,
+                      const Geometry& g, float* scores, const DeviceInfo& dev,
+                      cudaStream_t stream) {
+  if (nq == 0 || g.nb == 0) return QSA_OK;
+  qsa::ScoreProblem p{q, kb, scores, nq, H, D, g.nb, g.n_full, g.has_tail};
+  return qsa::launch_scores(p, dev, stream) == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qsa_abi_version(void) { return QSA_ABI_VERSION; }
+
+const char* qsa_status_str(qsa_status s) {
+  switch (s) {
+    case QSA_OK: return "QSA_OK";
+    case QSA_ERR_INVALID_ARG: return "QSA_ERR_INVALID_ARG";
+    case QSA_ERR_UNSUPPORTED_GEOMETRY: return "QSA_ERR_UNSUPPORTED_GEOMETRY";
+    case QSA_ERR_UNSUPPORTED_ARCH: return "QSA_ERR_UNSUPPORTED_ARCH";
+    case QSA_ERR_MISALIGNED: return "QSA_ERR_MISALIGNED";
+    case QSA_ERR_CUDA: return "QSA_ERR_CUDA";
+    case QSA_ERR_TIMEOUT: return "QSA_ERR_TIMEOUT";
+  }
+  return "QSA_ERR_UNKNOWN";
+}
+
+const char* qsa_arm(void) {
+  return "sm_103a: TMA + tcgen05.mma kind::f16 (M128, fp32 in TMEM) scorer with fused "
+         "ReLU/head-sum epilogue; fp32 pinned-order tail kernel (+1e9); radix top-k select "
+         "(block-index tie-break); cvt.rn fp32->fp16 stage";
+}
+
+int64_t qsa_num_blocks(int64_t n_kv, int32_t block) {
+  if (n_kv < 0 || block < 1) return -1;
+  return n_kv / block + (n_kv % block != 0 ? 1 : 0);
+}
+
+qsa_status qsa_f32_to_f16(const float* src, uint16_t* dst, int64_t n, qsa_stream_t stream) {
+  if (n < 0) return QSA_ERR_INVALID_ARG;
+  if (n == 0) return QSA_OK;
+  if (!src || !dst) return QSA_ERR_INVALID_ARG;
+  if (!aligned(src, 4) || !aligned(dst, 2)) return QSA_ERR_MISALIGNED;
+  const DeviceInfo* dev = nullptr;
+  qsa_status st = device_or_error(&dev);
+  if (st != QSA_OK) return st;
+  return qsa::launch_convert(src, dst, n, *dev, as_cuda(stream)) == cudaSuccess ? QSA_OK
+                                                                                 : QSA_ERR_CUDA;
+}
+
+qsa_status qsa_block_scores(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H,
+                            int32_t D, int64_t n_kv, int32_t block, float* scores,
+                            qsa_stream_t stream) {
+  Geometry g;
+  qsa_status st = check_scores(q, kb, nq, H, D, n_kv, block, scores, &g);
+  if (st != QSA_OK || nq == 0 || g.nb == 0) return st;
+  const DeviceInfo* dev = nullptr;
+  if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  return run_scores(q, kb, nq, H, D, g, scores, *dev, as_cuda(stream));
+}
+
+qsa_status qsa_select(const float* scores, int32_t nq, int32_t nb, int32_t k, int32_t* ids,
+                      qsa_stream_t stream) {
+  qsa_status st = check_select(scores, nq, nb, k, ids);
+  if (st != QSA_OK || nq == 0) return st;
+  const DeviceInfo* dev = nullptr;
+  if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  return qsa::launch_select(scores, nq, nb, k, ids, *dev, as_cuda(stream)) == cudaSuccess
+             ? QSA_OK
+             : QSA_ERR_CUDA;
+}
+
+qsa_status qsa_score_select(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H,
+                            int32_t D, int64_t n_kv, int32_t block, int32_t k, float* scores,
+                            int32_t* ids, qsa_stream_t stream) {
+  Geometry g;
+  qsa_status st = check_scores(q, kb, nq, H, D, n_kv, block, scores, &g);
+  if (st != QSA_OK) return st;
+  if ((st = check_select(scores, nq, g.nb, k, ids)) != QSA_OK) return st;
+  if (nq == 0) return QSA_OK;
+  const DeviceInfo* dev = nullptr;
+  if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  cudaStream_t s = as_cuda(stream);
+  if ((st = run_scores(q, kb, nq, H, D, g, scores, *dev, s)) != QSA_OK) return st;
+  return qsa::launch_select(scores, nq, static_cast<int32_t>(g.nb), k, ids, *dev, s) ==
+                 cudaSuccess
+             ? QSA_OK
+             : QSA_ERR_CUDA;
+}
+
+qsa_status qsa_select_step(const float* q32, uint16_t* q16, const uint16_t* kb, int32_t nq,
+                           int32_t H, int32_t D, int64_t n_kv, int32_t block, int32_t k,
+                           float* scores, int32_t* ids, qsa_stream_t stream) {
+  Geometry g;
+  qsa_status st = check_scores(q16, kb, nq, H, D, n_kv, block, scores, &g);
+  if (st != QSA_OK) return st;
+  if ((st = check_select(scores, nq, g.nb, k, ids)) != QSA_OK) return st;
+  if (nq == 0) return QSA_OK;
+  if (!q32 || !q16) return QSA_ERR_INVALID_ARG;
+  if (!aligned(q32, 4) || !aligned(q16, 16)) return QSA_ERR_MISALIGNED;
+  const DeviceInfo* dev = nullptr;
+  if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  cudaStream_t s = as_cuda(stream);
+  const int64_t n = static_cast<int64_t>(nq) * H * D;
+  if (qsa::launch_convert(q32, q16, n, *dev, s) != cudaSuccess) return QSA_ERR_CUDA;
+  if (g.nb == 0) {
+    return qsa::launch_select(scores, nq, 0, k, ids, *dev, s) == cudaSuccess ? QSA_OK
+                                                                             : QSA_ERR_CUDA;
+  }
+  if ((st = run_scores(q16, kb, nq, H, D, g, scores, *dev, s)) != QSA_OK) return st;
+  return qsa::launch_select(scores, nq, static_cast<int32_t>(g.nb), k, ids, *dev, s) ==
+                 cudaSuccess
+             ? QSA_OK
+             : QSA_ERR_CUDA;
+}
+
+qsa_status qsa_select_step_host(const float* q32_host, const uint16_t* kb_host, int32_t nq,
+                                int32_t H, int32_t D, int64_t n_kv, int32_t block, int32_t k,
+                                float* scores_host, int32_t* ids_host, float* q32_dev,
+                                uint16_t* q16_dev, uint16_t* kb_dev, float* scores_dev,
+                                int32_t* ids_dev, qsa_stream_t stream) {
+  Geometry g;
+  qsa_status st = check_scores(q16_dev, kb_dev, nq, H, D, n_kv, block, scores_dev, &g);
+  if (st != QSA_OK) return st;
+  if ((st = check_select(scores_dev, nq, g.nb, k, ids_dev)) != QSA_OK) return st;
+  if (nq == 0) return QSA_OK;
+  if (!q32_host || !ids_host || !q32_dev || !q16_dev || !ids_dev) return QSA_ERR_INVALID_ARG;
+  if (g.nb > 0 && (!kb_host || !scores_host)) return QSA_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  cudaStream_t s = as_cuda(stream);
+  const size_t q_bytes = static_cast<size_t>(nq) * H * D * sizeof(float);
+  const size_t kb_bytes = static_cast<size_t>(g.nb) * D * sizeof(uint16_t);
+  const size_t s_bytes = static_cast<size_t>(nq) * g.nb * sizeof(float);
+  const size_t id_bytes = static_cast<size_t>(nq) * k * sizeof(int32_t);
+  if (cudaMemcpyAsync(q32_dev, q32_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  if (kb_bytes &&
+      cudaMemcpyAsync(kb_dev, kb_host, kb_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  st = qsa_select_step(q32_dev, q16_dev, kb_dev, nq, H, D, n_kv, block, k, scores_dev, ids_dev,
+                       stream);
+  if (st != QSA_OK) return st;
+  if (s_bytes &&
+      cudaMemcpyAsync(scores_host, scores_dev, s_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  if (cudaMemcpyAsync(ids_host, ids_dev, id_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  return QSA_OK;
+}
+
+qsa_status qsa_device_status(int clear, uint32_t* bits, qsa_stream_t stream) {
+  const DeviceInfo* dev = nullptr;
+  qsa_status st = device_or_error(&dev);
+  if (st != QSA_OK) return st;
+  if (cudaStreamSynchronize(as_cuda(stream)) != cudaSuccess) return QSA_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, dev->status_word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  if (bits) *bits = v;
+  if (v != 0 && clear) {
+    if (cudaMemset(dev->status_word, 0, sizeof(uint32_t)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+      return QSA_ERR_CUDA;
+  }
+  return v == 0 ? QSA_OK : QSA_ERR_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// qsa_internal.h - host-side declarations shared by the C-ABI layer and the
+// kernel translation units. Not installed; not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace qsa {
+
+struct DeviceInfo {
+  int id = -1;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  int max_smem_optin = 0;
+  uint32_t* status_word = nullptr;  // device address of this device's status word
+  bool supported = false;           // compute capability 10.3
+  bool ready = false;               // kernel attributes set
+};
+
+// Info for the current device, initialised once per device (attributes of the
+// kernels are set then). Returns nullptr and sets *err on a CUDA failure.
+const DeviceInfo* current_device(cudaError_t* err);
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+// Per-TU one-time kernel attribute setup, called from current_device().
+cudaError_t init_score_kernels(const DeviceInfo& dev);
+cudaError_t init_select_kernels(const DeviceInfo& dev);
+
+// Launchers. Each returns cudaSuccess or the first CUDA error; arguments are
+// already validated by the caller.
+cudaError_t launch_convert(const float* src, uint16_t* dst, int64_t n, const DeviceInfo& dev,
+                           cudaStream_t stream);
+
+struct ScoreProblem {
+  const uint16_t* q;
+  const uint16_t* kb;
+  float* scores;
+  int32_t nq, H, D;
+  int64_t nb, n_full;
+  bool has_tail;
+};
+// Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
+cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStream_t stream);
+
+cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k, int32_t* ids,
+                          const DeviceInfo& dev, cudaStream_t stream);
+
+constexpr int kMaxSelectK = 1024;
+constexpr int kMaxSelectNb = 32768;
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s bound on any device-side wait
+
+}  // namespace qsa

@@ -1,0 +1,312 @@
+// score_tc.cu - QSA block scores on the sm_103a tensor cores, and the tail
+// block kernel.
+//
+// score(qi, b) = sum_h relu(sum_i kb[b, i] * q[qi, h, i])   (Strata pull request
+// 228, part 1, "qsa_block_scores_wmma": the multi-query block scorer).
+//
+// Full blocks: the contraction is the GEMM  Kb[n_full, D] x Q2[nq*H, D]^T  with
+// Q2 the [nq*H, D] view of q, computed swap-AB so that the 128 KV blocks of a
+// tile sit on the 128 TMEM lanes and the (query, head) pairs of the tile, head
+// fastest, sit on the TMEM columns. One CTA per (128-block, bn-column) tile:
+//   - thread 0 issues TMA loads of the tile's Kb rows and Q2 rows, one
+//     mbarrier per 64-wide K chunk (128-byte swizzled rows), then the
+//     tcgen05.mma kind::f16 steps (M=128, N=bn, K=16 each; fp16 in, fp32
+//     accumulate in TMEM) as each chunk lands, and one tcgen05.commit;
+//   - all four warps then read their 32 TMEM lanes (one KV block per thread),
+//     apply ReLU per head and sum the H adjacent columns of each query in
+//     registers, and store scores[qi, b] (a warp writes 32 consecutive b).
+// The [nq*H, n_full] pre-activation matrix never leaves TMEM and registers.
+//
+// Tail block (Strata pull request 856, "What": the shared tail kernel and the
+// +1e9 dead-tail rule): one thread per (query, head) sums the fp32 products
+// over i in order; one thread per query then sums max(acc_h, 0) over h in
+// order and adds 1e9f. Every step is a round-to-nearest-even fp32 operation
+// (no contraction, no reassociation), so the result is reproducible bit for
+// bit.
+#include <algorithm>
+
+#include "qsa_device.cuh"
+#include "qsa_internal.h"
+
+namespace qsa {
+
+constexpr int kTileM = 128;        // KV blocks per tile = MMA M = TMEM lanes
+constexpr int kKAtom = 64;         // fp16 elements per 128-byte swizzled row
+constexpr int kRowBytes = 128;
+constexpr int kScoreThreads = 128; // 4 warps = the 4 TMEM lane quarters
+constexpr int kTailThreads = 256;
+
+struct ScoreArgs {
+  float* scores;
+  int32_t nq, nb, n_full;
+  int32_t bn;          // TMEM columns (query-head pairs) per tile, multiple of 32
+  int32_t q_per_tile;  // bn / H
+  int32_t n_chunks;    // ceil(D / 64)
+  int32_t k_steps;     // D / 16
+  uint32_t tmem_cols;  // power of two >= bn
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+template <int H>
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    score_tc_kernel(const __grid_constant__ CUtensorMap tm_kb,
+                    const __grid_constant__ CUtensorMap tm_q, const ScoreArgs a) {
+  static_assert(32 % H == 0, "a 32-column TMEM load must hold whole queries");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint8_t* sA = smem;                                           // n_chunks x [128 rows x 128 B]
+  uint8_t* sB = sA + a.n_chunks * kTileM * kRowBytes;           // n_chunks x [bn rows x 128 B]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + a.n_chunks * a.bn * kRowBytes);
+  uint64_t* mma_bar = bars + a.n_chunks;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  volatile int* failed = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kTileM;
+  const int col0 = blockIdx.y * a.bn;
+
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < a.n_chunks; ++c) mbar_init(&bars[c], 1);
+    mbar_init(mma_bar, 1);
+    *failed = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tm_kb);
+    tma_prefetch_desc(&tm_q);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, a.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_d = *tmem_slot;
+
+  if (threadIdx.x == 0) {
+    const uint32_t chunk_bytes = static_cast<uint32_t>((kTileM + a.bn) * kRowBytes);
+    for (int c = 0; c < a.n_chunks; ++c) {
+      mbar_arrive_expect_tx(&bars[c], chunk_bytes);
+      tma_load_2d(sA + c * kTileM * kRowBytes, &tm_kb, c * kKAtom, m0, &bars[c]);
+      tma_load_2d(sB + c * a.bn * kRowBytes, &tm_q, c * kKAtom, col0, &bars[c]);
+    }
+    const uint32_t idesc = idesc_f16_f32(kTileM, a.bn);
+    bool ok = true;
+    for (int c = 0; c < a.n_chunks; ++c) {
+      if (!mbar_wait_bounded(&bars[c], 0, a.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t a_base = smem_u32(sA + c * kTileM * kRowBytes);
+      const uint32_t b_base = smem_u32(sB + c * a.bn * kRowBytes);
+#pragma unroll
+      for (int s = 0; s < kKAtom / 16; ++s) {
+        const int step = c * (kKAtom / 16) + s;
+        if (step < a.k_steps)
+          mma_f16_ss(tmem_d, smem_desc_k_sw128(a_base + s * 32), smem_desc_k_sw128(b_base + s * 32),
+                     idesc, step > 0 ? 1u : 0u);
+      }
+    }
+    mma_commit(mma_bar);  // arrives once every MMA issued above has completed
+    if (!ok) {
+      *failed = 1;
+      atomicOr(a.status, kErrScoreLoadTimeout);
+      // Loads may still be in flight into this CTA's shared memory: wait for
+      // them (bounded) before the CTA may finish.
+      for (int c = 0; c < a.n_chunks; ++c) mbar_wait_bounded(&bars[c], 0, a.timeout_ns);
+    }
+  }
+  __syncwarp();
+
+  if (!mbar_wait_bounded(mma_bar, 0, a.timeout_ns)) {
+    *failed = 1;
+    if (lane == 0) atomicOr(a.status, kErrScoreMmaTimeout);
+  }
+  __syncthreads();
+  if (*failed == 0) {
+    tc_fence_after_sync();
+    const int lane_base = (warp & 3) * 32;
+    const int b = m0 + lane_base + lane;
+    const bool b_ok = b < a.n_full;
+    float* out = a.scores + b;
+    const int q0 = blockIdx.y * a.q_per_tile;
+    constexpr int kQPerLoad = 32 / H;
+    for (int c0 = 0; c0 < a.bn; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld_32cols(tmem_d + (static_cast<uint32_t>(lane_base) << 16) + c0, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < kQPerLoad; ++j) {
+        float s = 0.0f;
+#pragma unroll
+        for (int h = 0; h < H; ++h) s = __fadd_rn(s, fmaxf(__uint_as_float(r[j * H + h]), 0.0f));
+        const int qidx = q0 + c0 / H + j;
+        if (b_ok && qidx < a.nq) out[static_cast<size_t>(qidx) * a.nb] = s;
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem_d, a.tmem_cols);
+}
+
+__global__ void __launch_bounds__(kTailThreads)
+    tail_kernel(const __half* __restrict__ q, const __half* __restrict__ kb_tail,
+                float* __restrict__ scores, int32_t nq, int32_t H, int32_t D, int64_t nb) {
+  __shared__ float acc_s[kTailThreads];
+  const int q_per_block = kTailThreads / H;
+  const int ql = threadIdx.x / H;
+  const int h = threadIdx.x - ql * H;
+  const int64_t qi = static_cast<int64_t>(blockIdx.x) * q_per_block + ql;
+  const bool active = ql < q_per_block && qi < nq;
+  float acc = 0.0f;
+  if (active) {
+    const __half* qr = q + (qi * H + h) * D;
+    for (int i = 0; i < D; i += 8) {
+      const uint4 qv = *reinterpret_cast<const uint4*>(qr + i);
+      const uint4 kv = *reinterpret_cast<const uint4*>(kb_tail + i);
+      const __half* qh = reinterpret_cast<const __half*>(&qv);
+      const __half* kh = reinterpret_cast<const __half*>(&kv);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        acc = __fadd_rn(acc, __fmul_rn(__half2float(qh[j]), __half2float(kh[j])));
+    }
+  }
+  acc_s[threadIdx.x] = acc;
+  __syncthreads();
+  if (active && h == 0) {
+    float t = 0.0f;
+    for (int hh = 0; hh < H; ++hh) t = __fadd_rn(t, fmaxf(acc_s[ql * H + hh], 0.0f));
+    scores[qi * nb + (nb - 1)] = __fadd_rn(t, 1.0e9f);
+  }
+}
+
+// ------------------------------------------------------------------ host
+namespace {
+
+uint32_t tmem_cols_for(int bn) {
+  uint32_t c = 32;
+  while (c < static_cast<uint32_t>(bn)) c <<= 1;
+  return c;
+}
+
+// Dynamic shared memory for one CTA: operand tiles, barriers, slack for the
+// 1024-byte alignment; then padded so that no more CTAs fit on an SM than its
+// 512 TMEM columns can serve at once.
+size_t score_smem_bytes(int bn, int n_chunks, uint32_t tmem_cols) {
+  size_t need = static_cast<size_t>(n_chunks) * (kTileM + bn) * kRowBytes +
+                (n_chunks + 1) * sizeof(uint64_t) + 16 + 1024;
+  const size_t max_ctas = 512 / tmem_cols;
+  const size_t per_sm = 233472;  // 228 KB of shared memory per SM
+  const size_t floor_bytes = per_sm / (max_ctas + 1) + 1;
+  return std::max(need, floor_bytes);
+}
+
+template <int H>
+const void* score_kernel_ptr() {
+  return reinterpret_cast<const void*>(&score_tc_kernel<H>);
+}
+
+const void* score_kernel_for(int H) {
+  switch (H) {
+    case 1: return score_kernel_ptr<1>();
+    case 2: return score_kernel_ptr<2>();
+    case 4: return score_kernel_ptr<4>();
+    case 8: return score_kernel_ptr<8>();
+    case 16: return score_kernel_ptr<16>();
+    case 32: return score_kernel_ptr<32>();
+    default: return nullptr;
+  }
+}
+
+bool encode_2d_f16(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows,
+                   uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Columns per tile: the widest of 256/128/64/32 that still gives at least one
+// CTA per SM; narrower tiles spread small problems over more SMs.
+int choose_bn(int64_t m_tiles, int64_t cols, int sm_count) {
+  for (int bn : {256, 128, 64}) {
+    const int64_t n_tiles = (cols + bn - 1) / bn;
+    if (m_tiles * n_tiles >= sm_count) return bn;
+  }
+  return 32;
+}
+
+}  // namespace
+
+cudaError_t init_score_kernels(const DeviceInfo& dev) {
+  const size_t max_smem = static_cast<size_t>(dev.max_smem_optin);
+  for (int H : {1, 2, 4, 8, 16, 32}) {
+    cudaError_t e = cudaFuncSetAttribute(score_kernel_for(H),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(max_smem));
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStream_t stream) {
+  if (p.nq > 0 && p.n_full > 0) {
+    const int64_t cols = static_cast<int64_t>(p.nq) * p.H;
+    const int64_t m_tiles = (p.n_full + kTileM - 1) / kTileM;
+    const int bn = choose_bn(m_tiles, cols, dev.sm_count);
+    const int64_t n_tiles = (cols + bn - 1) / bn;
+    if (m_tiles > 0x7FFFFFFF || n_tiles > 65535) return cudaErrorInvalidValue;
+    CUtensorMap tm_kb, tm_q;
+    if (!encode_2d_f16(&tm_kb, p.kb, p.D, p.n_full, kKAtom, kTileM) ||
+        !encode_2d_f16(&tm_q, p.q, p.D, cols, kKAtom, bn))
+      return cudaErrorInvalidValue;
+    ScoreArgs a;
+    a.scores = p.scores;
+    a.nq = p.nq;
+    a.nb = static_cast<int32_t>(p.nb);
+    a.n_full = static_cast<int32_t>(p.n_full);
+    a.bn = bn;
+    a.q_per_tile = bn / p.H;
+    a.n_chunks = (p.D + kKAtom - 1) / kKAtom;
+    a.k_steps = p.D / 16;
+    a.tmem_cols = tmem_cols_for(bn);
+    a.status = dev.status_word;
+    a.timeout_ns = kWaitTimeoutNs;
+    const size_t smem = score_smem_bytes(bn, a.n_chunks, a.tmem_cols);
+    if (smem > static_cast<size_t>(dev.max_smem_optin)) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(m_tiles), static_cast<unsigned>(n_tiles));
+    const dim3 block(kScoreThreads);
+    switch (p.H) {
+      case 1: score_tc_kernel<1><<<grid, block, smem, stream>>>(tm_kb, tm_q, a); break;
+      case 2: score_tc_kernel<2><<<grid, block, smem, stream>>>(tm_kb, tm_q, a); break;
+      case 4: score_tc_kernel<4><<<grid, block, smem, stream>>>(tm_kb, tm_q, a); break;
+      case 8: score_tc_kernel<8><<<grid, block, smem, stream>>>(tm_kb, tm_q, a); break;
+      case 16: score_tc_kernel<16><<<grid, block, smem, stream>>>(tm_kb, tm_q, a); break;
+      case 32: score_tc_kernel<32><<<grid, block, smem, stream>>>(tm_kb, tm_q, a); break;
+      default: return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (p.nq > 0 && p.has_tail) {
+    const int q_per_block = kTailThreads / p.H;
+    const int64_t grid = (p.nq + q_per_block - 1) / q_per_block;
+    tail_kernel<<<static_cast<unsigned>(grid), kTailThreads, 0, stream>>>(
+        reinterpret_cast<const __half*>(p.q),
+        reinterpret_cast<const __half*>(p.kb) + (p.nb - 1) * p.D, p.scores, p.nq, p.H, p.D, p.nb);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
+}  // namespace qsa
