@@ -1,0 +1,484 @@
+#!/usr/bin/env python
+"""Benchmark of the QSA selection step on GB300: query*blocks per second.
+
+One step = one pass of the hot path over one query batch: the f32 queries
+are converted to fp16, every block is scored (tensor-core full blocks, the
+fp32 tail block with the +1e9 bonus) and the top-k blocks are selected per
+query. Inputs are synthetic (qsa_inputs), resident in HBM, and the step
+rotates through enough distinct input/output sets (> 2 x the 129 MB L2) that
+every step reads its operands from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, on the host cores
+
+Under torchrun every rank runs its own batches on its own GPU (no collective
+on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import qsa_inputs as qi  # noqa: E402
+
+METRIC = "QSA score+top-k query·blocks/sec at 128K ctx, nq=256; % of GB300 roofline"
+UNIT = "query*blocks/s"
+DEFAULT_WORKLOAD = "long128k_nq256_h8_d128_kv131072"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by kernel, with the SHA-256 of the kernel's
+# source file at capture time; a stale entry reports null.
+NCU_TRAFFIC = {}
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(qi.BY_NAME))
+    p.add_argument("--min-timed-seconds", type=float, default=1.0,
+                   help="repeat the K-step timed region until this much time has passed")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle baseline budget")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": w.name, "nq": w.nq, "H": w.H, "D": w.D, "n_kv": w.n_kv, "block": w.block,
+           "nb": w.nb, "k": w.k, "q_input": "f32, converted to fp16 on the device in the step",
+           "kb": "fp16, resident"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def units_per_step(w):
+    return w.nq * w.nb
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="qsa_clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, smax = [], []
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                pass
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# -------------------------------------------------------------- GPU helpers
+class Sets:
+    """Rotating device buffer sets for one workload."""
+
+    def __init__(self, torch, tbs, w, device, min_bytes):
+        per = (w.nq * w.H * w.D * (4 + 2) + w.nb * w.D * 2 + w.nq * w.nb * 4 + w.nq * w.k * 4)
+        self.n = max(2, math.ceil(min_bytes / per))
+        self.per_set_bytes = per
+        self.q32, self.q16, self.kb, self.scores, self.ids = [], [], [], [], []
+        for v in range(self.n):
+            q32, _ = qi.make_f32_inputs(w, variant=v)
+            _, kb = qi.make_inputs(w, variant=v)
+            self.q32.append(torch.from_numpy(q32).to(device))
+            self.kb.append(torch.from_numpy(kb).to(device))
+            self.q16.append(torch.empty((w.nq, w.H, w.D), dtype=torch.float16, device=device))
+            self.scores.append(torch.empty((w.nq, w.nb), dtype=torch.float32, device=device))
+            self.ids.append(torch.empty((w.nq, w.k), dtype=torch.int32, device=device))
+        # every q16 holds a converted copy so the score-only and select-only
+        # timings read real data
+        for v in range(self.n):
+            tbs.qsa_f32_to_f16(self.q32[v], out=self.q16[v])
+        torch.cuda.synchronize()
+
+
+def graph_of(torch, stream, fn, count):
+    """Capture `count` calls fn(i) into one CUDA graph on `stream`."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(count):
+                fn(i)
+    return g
+
+
+def time_region(torch, stream, replay, reps_min, seconds, barrier=None):
+    """Time replay() (exactly K steps) with CUDA events on `stream`, repeated
+    until `seconds` have passed (at least reps_min times). Returns the list of
+    elapsed milliseconds, each the max over ranks."""
+    out = []
+    t_end = time.perf_counter() + seconds
+    while len(out) < reps_min or time.perf_counter() < t_end:
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if barrier:
+            ms = barrier(ms)
+        out.append(ms)
+        if len(out) >= 200:
+            break
+    return out
+
+
+def kernel_source_sha(name):
+    path = os.path.join(ROOT, "top_block_selection_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel, source, w):
+    e = NCU_TRAFFIC.get(kernel)
+    if not e or e.get("source_sha") != kernel_source_sha(source) or e.get("workload") != w.name:
+        return None
+    return e["bytes_per_launch"]
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+    import top_block_selection_gb300 as tbs
+    from top_block_selection_gb300 import _build
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier(ms=None):
+        if dist is None:
+            return ms
+        if ms is None:
+            dist.barrier()
+            return None
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    if rank == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    _build.build()
+    tbs.load_library()
+    w = qi.BY_NAME[args.workload]
+    K, W = args.steps, args.warmup
+    if K < 1 or W < 3:
+        raise SystemExit("need --steps >= 1 and --warmup >= 3")
+    sets = Sets(torch, tbs, w, device, 2 * L2_BYTES)
+    stream = torch.cuda.Stream(device)
+    peaks, peak_src = load_peaks()
+
+    def step(i):
+        v = i % sets.n
+        tbs.qsa_select_step(sets.q32[v], sets.kb[v], w.n_kv, w.k, w.block,
+                            q16=sets.q16[v], scores=sets.scores[v], ids=sets.ids[v])
+
+    def score_only(i):
+        v = i % sets.n
+        tbs.qsa_block_scores(sets.q16[v], sets.kb[v], w.n_kv, w.block, out=sets.scores[v])
+
+    def select_only(i):
+        v = i % sets.n
+        tbs.qsa_select(sets.scores[v], w.k, out=sets.ids[v])
+
+    def convert_only(i):
+        v = i % sets.n
+        tbs.qsa_f32_to_f16(sets.q32[v], out=sets.q16[v])
+
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(i)
+    torch.cuda.synchronize()
+
+    # CUDA graphs of exactly K calls each (captured once, replayed)
+    graphs = {name: graph_of(torch, stream, fn, K) for name, fn in
+              (("step", step), ("score", score_only), ("select", select_only), ("convert", convert_only))}
+    replays = {}
+    for name, g in graphs.items():  # upload + one untimed replay, on the timed stream
+        def rp(g=g):
+            with torch.cuda.stream(stream):
+                g.replay()
+        replays[name] = rp
+        rp()
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    step_ms = time_region(torch, stream, replays["step"], 5, args.min_timed_seconds, barrier if dist else None)
+    clocks = sampler.stop()
+    kern_ms = {name: statistics.median(time_region(torch, stream, replays[name], 5, 0.3))
+               for name in ("score", "select", "convert")}
+
+    ms_step = statistics.median(step_ms) / K
+    value = world * units_per_step(w) * K / (statistics.median(step_ms) / 1e3)
+
+    # roofline of each kernel, per launch
+    flops_score = 2.0 * w.nq * w.H * w.D * w.n_full
+    bytes_score = 2.0 * w.nq * w.H * w.D + 2.0 * w.n_full * w.D + 4.0 * w.nq * w.nb
+    bytes_select = 4.0 * w.nq * w.nb + 4.0 * w.nq * w.k
+    bytes_convert = 6.0 * w.nq * w.H * w.D
+    t = {n: kern_ms[n] / K / 1e3 for n in kern_ms}
+    kernels = {
+        "score": {"bound": "tensor" if flops_score / (peaks["bf16_tflops"] * 1e12) > bytes_score / (peaks["hbm_gbs"] * 1e9) else "hbm",
+                  "us_per_launch": t["score"] * 1e6,
+                  "tflops": flops_score / t["score"] / 1e12, "gbs": bytes_score / t["score"] / 1e9},
+        "select": {"bound": "hbm", "us_per_launch": t["select"] * 1e6, "gbs": bytes_select / t["select"] / 1e9},
+        "convert": {"bound": "hbm", "us_per_launch": t["convert"] * 1e6, "gbs": bytes_convert / t["convert"] / 1e9},
+    }
+    dom = max(kernels, key=lambda n: kernels[n]["us_per_launch"])
+    if dom == "score" and kernels["score"]["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": kernels["score"]["tflops"], "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "traffic": traffic_for("score_tc_kernel", "score_tc.cu", w)}
+        roof_kernel = "score_tc_kernel (qsa_block_scores)"
+    else:
+        gbs = kernels[dom]["gbs"]
+        src = {"score": "score_tc.cu", "select": "select.cu", "convert": "convert.cu"}[dom]
+        kname = {"score": "score_tc_kernel", "select": "select_kernel", "convert": "convert_vec8_kernel"}[dom]
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "traffic": traffic_for(kname, src, w)}
+        roof_kernel = kname
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = roof_kernel
+    roof["peak_source"] = f"{peak_src} (burst; kernel timed alone)"
+
+    # whole-step roofline: max(FLOPs / P, bytes / BW) with the algorithmic
+    # FLOPs of every block and the bytes each input and output moves once (f32
+    # q read, kb read, scores and ids written)
+    step_flops = 2.0 * w.nq * w.H * w.D * w.nb
+    step_bytes = 4.0 * w.nq * w.H * w.D + 2.0 * w.nb * w.D + 4.0 * w.nq * w.nb + 4.0 * w.nq * w.k
+    t_roof = max(step_flops / (peaks["bf16_tflops"] * 1e12), step_bytes / (peaks["hbm_gbs"] * 1e9))
+
+    # end-to-end through the host-buffer entry point
+    e2e = run_e2e(torch, tbs, w, device, stream, K, W, barrier if dist else None)
+
+    launches_per_step = 1 + (1 if w.n_full > 0 else 0) + (1 if w.has_tail else 0) + 1
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": workload_config(w, {
+            "parallelism": f"replicas x{world} (independent query batches per GPU)",
+            "l2": f"rotating {sets.n} distinct input/output sets ({sets.n * sets.per_set_bytes / 2**20:.0f} MiB > 2x L2)",
+            "timing": f"CUDA graph of {K} steps; CUDA events on the launching stream; median of "
+                      f"{len(step_ms)} repetitions",
+            "accumulate": "fp32"}),
+        "roofline": roof,
+        "step_roofline": {"flops": step_flops, "bytes": step_bytes, "t_roofline_us": t_roof * 1e6,
+                          "t_step_us": ms_step * 1e3, "frac": t_roof / (ms_step / 1e3)},
+        "kernels": kernels,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(torch, tbs, w, device, stream, K, W, barrier):
+    """Same metric through qsa_select_step_host: each step copies its f32
+    queries and fp16 keys from pinned host memory, runs the step and copies
+    scores and ids back, all on one stream; events bracket the K steps."""
+    hosts = []
+    for v in range(2):
+        q32, _ = qi.make_f32_inputs(w, variant=v)
+        _, kb = qi.make_inputs(w, variant=v)
+        hosts.append((torch.from_numpy(q32).pin_memory(), torch.from_numpy(kb).pin_memory(),
+                      torch.empty((w.nq, w.nb), dtype=torch.float32).pin_memory(),
+                      torch.empty((w.nq, w.k), dtype=torch.int32).pin_memory()))
+    bufs = (torch.empty((w.nq, w.H, w.D), dtype=torch.float32, device=device),
+            torch.empty((w.nq, w.H, w.D), dtype=torch.float16, device=device),
+            torch.empty((w.nb, w.D), dtype=torch.float16, device=device),
+            torch.empty((w.nq, w.nb), dtype=torch.float32, device=device),
+            torch.empty((w.nq, w.k), dtype=torch.int32, device=device))
+
+    def one(i):
+        h = hosts[i % 2]
+        tbs.qsa_select_step_host(h[0], h[1], w.n_kv, w.k, w.block, h[2], h[3], bufs, stream=stream)
+
+    for i in range(W):
+        one(i)
+    torch.cuda.synchronize()
+
+    def replay():
+        for i in range(K):
+            one(i)
+
+    ms = time_region(torch, stream, replay, 3, 0.5, barrier)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    med = statistics.median(ms)
+    return {"value": world * units_per_step(w) * K / (med / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": w.nq * w.H * w.D * 4 + w.nb * w.D * 2,
+            "d2h_bytes_per_step": w.nq * w.nb * 4 + w.nq * w.k * 4,
+            "ms_per_step": med / K, "api": "qsa_select_step_host (pinned host buffers, eager calls)"}
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_step(orc, w, q32, kb, nq_sample=None):
+    """The oracle as it stands on one batch (or its first nq_sample queries):
+    fp16 conversion of q, float64 scores, the fp32 tail, lexsort top-k."""
+    if nq_sample is not None:
+        q32 = q32[:nq_sample]
+    q16 = orc.f32_to_f16(q32)
+    s = orc.scores_f64(q16, kb, w.n_kv, w.block)
+    tail = orc.tail_scores_f32(q16, kb, w.n_kv, w.block)
+    if tail is not None:
+        s[:, -1] = tail
+    return orc.select_topk(s, w.k)
+
+
+def cpu_baseline(w, seconds):
+    from oracle import qsa_oracle as orc
+    q32, _ = qi.make_f32_inputs(w)
+    _, kb = qi.make_inputs(w)
+    oracle_step(orc, w, q32, kb)                  # warm
+    n, t0 = 0, time.perf_counter()
+    while n < 3 or time.perf_counter() - t0 < seconds:
+        oracle_step(orc, w, q32, kb)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": n * units_per_step(w) / dt, "unit": UNIT, "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{n} whole {w.nq}-query batches of {w.name} in {dt:.1f} s (numpy float64 "
+                      f"scores, fp32 tail, lexsort top-{w.k}; BLAS threads = all {os.cpu_count()} cores)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    from oracle import qsa_oracle as orc
+    w = qi.BY_NAME[args.workload]
+    K, W = args.steps, args.warmup
+    nq_s = min(w.nq, 16)
+    q32, _ = qi.make_f32_inputs(w)
+    _, kb = qi.make_inputs(w)
+    for _ in range(W):
+        oracle_step(orc, w, q32, kb, nq_s)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        oracle_step(orc, w, q32, kb, nq_s)
+    dt = time.perf_counter() - t0
+    units = nq_s * w.nb
+    value = units * K / dt
+    sample = (f"each step: the first {nq_s} of the {w.nq} queries of {w.name} (numpy float64 "
+              f"scores, fp32 tail, lexsort top-{w.k}); BLAS threads = all {os.cpu_count()} cores")
+    res = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+           "ms_per_step": dt / K * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+           "config": workload_config(w, {"parallelism": "host cores (CPU oracle)"}),
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -63,8 +63,15 @@ def _f16(x: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float16))
 
 
-def make_inputs(w: Workload):
+def _seed(w: Workload, variant: int, salt: int = 0) -> int:
+    return w.seed + salt + 104729 * variant
+
+
+def make_inputs(w: Workload, variant: int = 0):
     """Return (q f16 [nq,H,D], kb f16 [nb,D]) for workload ``w``.
+
+    ``variant`` > 0 draws another input set of the same recipe (distinct
+    buffers for benchmarks that rotate through more data than L2 holds).
 
     normal1:          q, kb ~ N(0, 1)
     normal_d:         q, kb ~ N(0, 1/sqrt(D)) (standard deviation 1/sqrt(D))
@@ -74,7 +81,7 @@ def make_inputs(w: Workload):
                       second chosen row is forced onto the first one's
                       coordinate so that exact score ties exist.
     """
-    rng = np.random.default_rng(w.seed)
+    rng = np.random.default_rng(_seed(w, variant))
     nb = w.nb
     if w.dist == "normal1":
         sd = 1.0
@@ -97,13 +104,13 @@ def make_inputs(w: Workload):
     return _f16(q), _f16(kb)
 
 
-def make_f32_inputs(w: Workload):
+def make_f32_inputs(w: Workload, variant: int = 0):
     """Workload inputs as the f32 arrays that feed the fp32->fp16 stage.
 
     The f32 values are the drawn float64 values rounded to float32 (not to
     fp16), so the conversion stage has real rounding work to do.
     """
-    rng = np.random.default_rng(w.seed + 7919)
+    rng = np.random.default_rng(_seed(w, variant, 7919))
     sd = 1.0 if w.dist == "normal1" else 1.0 / math.sqrt(w.D)
     scale = 8.0 if w.dist == "normal_d_x8" else 1.0
     q = rng.normal(0.0, sd, size=(w.nq, w.H, w.D)) * scale
