@@ -68,6 +68,10 @@ const char* qsa_status_str(qsa_status status);
  * part 1, which prints the arm that ran). */
 const char* qsa_arm(void);
 
+/* Static text of the last CUDA error that made a call of this thread return
+ * QSA_ERR_CUDA ("no error" if none has). */
+const char* qsa_last_cuda_error(void);
+
 /* nb = ceil(n_kv / block): the number of KV blocks, the tail included.
  * Returns -1 if n_kv < 0 or block < 1. */
 int64_t qsa_num_blocks(int64_t n_kv, int32_t block);
@@ -130,9 +134,10 @@ qsa_status qsa_select(const float* scores, int32_t nq, int32_t nb, int32_t k, in
                       qsa_stream_t stream);
 
 /*
- * qsa_score_select - the metric path: qsa_block_scores followed by qsa_select
- * on the same stream, with the same arguments and rules as those two. Both
- * outputs are written: scores [nq, nb] and ids [nq, k].
+ * qsa_score_select - the metric path in one launch: the results of
+ * qsa_block_scores and then qsa_select, with the same arguments and rules as
+ * those two (and bit-identical results). Both outputs are written: scores
+ * [nq, nb] and ids [nq, k].
  */
 qsa_status qsa_score_select(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H,
                             int32_t D, int64_t n_kv, int32_t block, int32_t k, float* scores,
@@ -140,11 +145,14 @@ qsa_status qsa_score_select(const uint16_t* q, const uint16_t* kb, int32_t nq, i
 
 /*
  * qsa_select_step - one whole pass of the selection phase for one query
- * batch: q arrives as f32, is converted to fp16 into the caller's q16 buffer
- * (qsa_f32_to_f16), then scored and selected (qsa_score_select).
+ * batch, in one launch: q arrives as f32 and is rounded to fp16 (as by
+ * qsa_f32_to_f16) on its way into the tensor cores, then every block is
+ * scored and the top-k selected (as by qsa_score_select).
  *
- *   q32  f32 [nq, H, D] device; q16 f16 [nq, H, D] device, 16-byte aligned,
- *   written by the call; the other arguments as for qsa_score_select.
+ *   q32  f32 [nq, H, D] device, 16-byte aligned.
+ *   q16  optional: NULL, or f16 [nq, H, D] device, 16-byte aligned, which
+ *        then receives the converted queries.
+ *   The other arguments as for qsa_score_select.
  */
 qsa_status qsa_select_step(const float* q32, uint16_t* q16, const uint16_t* kb, int32_t nq,
                            int32_t H, int32_t D, int64_t n_kv, int32_t block, int32_t k,

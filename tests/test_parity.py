@@ -129,6 +129,41 @@ def test_write_set_canaries(tbs):
     assert not np.any(ib[guard:-guard] == 0x5A5A5A5A)
 
 
+@pytest.mark.parametrize("nq,H,nb,tail,k", [(9, 8, 3077, True, 40), (20, 4, 8 * 128 * 3, False, 64),
+                                            (3, 8, 32768, True, 64), (37, 16, 1100, True, 100),
+                                            (5, 1, 2500, False, 33), (70, 2, 1500, True, 1024)])
+def test_many_tiles_per_cta(tbs, nq, H, nb, tail, k):
+    """More than two 128-block tiles per CTA (the Kb stages and the TMEM
+    accumulators are reused), partial query groups, and long rows."""
+    q, kb = qi.random_case(nq, H, 128, nb, seed=nq * 13 + nb, scale=0.25)
+    check_case(tbs, q, kb, nb * 64 - (21 if tail else 0), 64, k, f"tiles-{nq}-{H}-{nb}")
+
+
+def test_fused_matches_separate_kernels(tbs):
+    """The fused launch and the separate score + select kernels agree bit for bit."""
+    for w in qi.WORKLOADS[:4]:
+        q, kb = qi.make_inputs(w)
+        qd, kd = dev(q), dev(kb)
+        s_f, i_f = tbs.qsa_score_select(qd, kd, w.n_kv, w.k, w.block)
+        s_u = tbs.qsa_block_scores(qd, kd, w.n_kv, w.block)
+        i_u = tbs.qsa_select(s_u, w.k)
+        torch.cuda.synchronize()
+        assert torch.equal(s_f.view(torch.int32), s_u.view(torch.int32)), w.name
+        assert torch.equal(i_f, i_u), w.name
+
+
+def test_select_step_without_q16_output(tbs):
+    w = qi.WORKLOADS[0]
+    q32, _ = qi.make_f32_inputs(w)
+    _, kb = qi.make_inputs(w)
+    q16 = torch.empty(q32.shape, dtype=torch.float16, device="cuda")
+    a = tbs.qsa_select_step(dev(q32), dev(kb), w.n_kv, w.k, w.block, q16=q16)
+    b = tbs.qsa_select_step(dev(q32), dev(kb), w.n_kv, w.k, w.block)
+    torch.cuda.synchronize()
+    assert b[0] is None
+    assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32)) and torch.equal(a[2], b[2])
+
+
 def test_determinism_double_launch(tbs):
     w = qi.WORKLOADS[3]
     q, kb = qi.make_inputs(w)
@@ -180,7 +215,9 @@ def test_select_step_from_f32(tbs, w):
     exercises the 2^-9.5 * S operand-rounding term of the bound."""
     q32, kb32 = qi.make_f32_inputs(w)
     kb16_gpu = tbs.qsa_f32_to_f16(dev(kb32))
-    q16_gpu, s_gpu, ids_gpu = tbs.qsa_select_step(dev(q32), kb16_gpu, w.n_kv, w.k, w.block)
+    q16_buf = torch.empty(q32.shape, dtype=torch.float16, device="cuda")
+    q16_gpu, s_gpu, ids_gpu = tbs.qsa_select_step(dev(q32), kb16_gpu, w.n_kv, w.k, w.block,
+                                                  q16=q16_buf)
     torch.cuda.synchronize()
     kb16 = orc.f32_to_f16(kb32)
     assert np.array_equal(kb16_gpu.cpu().numpy().view(np.uint16), kb16.view(np.uint16))
@@ -216,6 +253,7 @@ def test_select_step_host_matches_device(tbs):
     torch.cuda.synchronize()
     assert np.array_equal(sh.numpy().view(np.uint32), s_d.cpu().numpy().view(np.uint32))
     assert np.array_equal(ih.numpy(), i_d.cpu().numpy())
+    assert np.array_equal(bufs[1].cpu().numpy().view(np.uint16), orc.f32_to_f16(q32).view(np.uint16))
 
 
 def test_negative_control_on_gpu_scores(tbs):

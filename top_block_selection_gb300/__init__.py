@@ -13,7 +13,8 @@ import ctypes
 import os
 
 __all__ = [
-    "QsaError", "load_library", "library_path", "qsa_abi_version", "qsa_status_str", "qsa_arm",
+    "QsaError", "load_library", "library_path", "qsa_abi_version", "qsa_status_str",
+    "qsa_last_cuda_error", "qsa_arm",
     "qsa_num_blocks", "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select",
     "qsa_select_step", "qsa_select_step_host", "qsa_device_status", "EXPORTED_SYMBOLS",
 ]
@@ -23,8 +24,8 @@ _LIB = None
 
 # Every symbol declared in include/qsa.h.
 EXPORTED_SYMBOLS = (
-    "qsa_abi_version", "qsa_status_str", "qsa_arm", "qsa_num_blocks", "qsa_f32_to_f16",
-    "qsa_block_scores", "qsa_select", "qsa_score_select", "qsa_select_step",
+    "qsa_abi_version", "qsa_status_str", "qsa_last_cuda_error", "qsa_arm", "qsa_num_blocks",
+    "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select", "qsa_select_step",
     "qsa_select_step_host", "qsa_device_status",
 )
 
@@ -36,9 +37,10 @@ STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED_G
 class QsaError(RuntimeError):
     """A libqsa entry point returned a status other than QSA_OK."""
 
-    def __init__(self, status: int, where: str):
+    def __init__(self, status: int, where: str, detail: str = ""):
         self.status = status
-        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+        msg = f"{where}: {STATUS_NAMES.get(status, status)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
 
 
 def library_path() -> str:
@@ -60,6 +62,7 @@ def load_library():
         "qsa_abi_version": (ctypes.c_int, []),
         "qsa_status_str": (ctypes.c_char_p, [ctypes.c_int]),
         "qsa_arm": (ctypes.c_char_p, []),
+        "qsa_last_cuda_error": (ctypes.c_char_p, []),
         "qsa_num_blocks": (i64, [i64, i32]),
         "qsa_f32_to_f16": (ctypes.c_int, [vp, vp, i64, vp]),
         "qsa_block_scores": (ctypes.c_int, [vp, vp, i32, i32, i32, i64, i32, vp, vp]),
@@ -81,7 +84,8 @@ def load_library():
 # ------------------------------------------------------------------ helpers
 def _check(status: int, where: str):
     if status != 0:
-        raise QsaError(status, where)
+        detail = _LIB.qsa_last_cuda_error().decode() if status == 5 and _LIB is not None else ""
+        raise QsaError(status, where, detail)
 
 
 def _torch():
@@ -114,6 +118,10 @@ def qsa_abi_version() -> int:
 
 def qsa_status_str(status: int) -> str:
     return load_library().qsa_status_str(status).decode()
+
+
+def qsa_last_cuda_error() -> str:
+    return load_library().qsa_last_cuda_error().decode()
 
 
 def qsa_arm() -> str:
@@ -212,8 +220,9 @@ def qsa_score_select(q, kb, n_kv: int, k: int, block: int = 64, scores=None, ids
 
 
 def qsa_select_step(q32, kb, n_kv: int, k: int, block: int = 64, q16=None, scores=None, ids=None):
-    """One selection step from f32 queries: convert, score, select.
-    Returns (q16, scores, ids)."""
+    """One selection step from f32 queries in one fused launch: fp16
+    conversion, scores, select. q16, if given, receives the converted
+    queries; otherwise they stay on chip. Returns (q16 or None, scores, ids)."""
     torch = _torch()
     _need(q32, torch.float32, 3, "q32")
     _need(kb, torch.float16, 2, "kb")
@@ -221,26 +230,30 @@ def qsa_select_step(q32, kb, n_kv: int, k: int, block: int = 64, q16=None, score
     nb = qsa_num_blocks(n_kv, block)
     if nb < 0 or kb.shape[1] != D or kb.shape[0] < nb:
         raise ValueError("kb must be [>= nb, D] and n_kv >= 0, block >= 1")
-    if q16 is None:
-        q16 = torch.empty((nq, H, D), dtype=torch.float16, device=q32.device)
     if scores is None:
         scores = torch.empty((nq, nb), dtype=torch.float32, device=q32.device)
     if ids is None:
         ids = torch.empty((nq, k), dtype=torch.int32, device=q32.device)
-    _need(q16, torch.float16, 3, "q16")
+    if q16 is not None:
+        _need(q16, torch.float16, 3, "q16")
+        if tuple(q16.shape) != (nq, H, D):
+            raise ValueError("q16 must be shaped like q32")
     _need(scores, torch.float32, 2, "scores")
     _need(ids, torch.int32, 2, "ids")
+    if tuple(scores.shape) != (nq, nb) or tuple(ids.shape) != (nq, k):
+        raise ValueError("scores must be [nq, nb] and ids [nq, k]")
     lib = load_library()
     with torch.cuda.device(q32.device):
-        _check(lib.qsa_select_step(_ptr(q32), _ptr(q16), _ptr(kb), nq, H, D, n_kv, block, k,
-                                   _ptr(scores), _ptr(ids), _stream_of(q32)), "qsa_select_step")
+        _check(lib.qsa_select_step(_ptr(q32), _ptr(q16) if q16 is not None else None, _ptr(kb), nq,
+                                   H, D, n_kv, block, k, _ptr(scores), _ptr(ids), _stream_of(q32)),
+               "qsa_select_step")
     return q16, scores, ids
 
 
 def qsa_select_step_host(q32_host, kb_host, n_kv: int, k: int, block: int, scores_host, ids_host,
                          dev_buffers, stream=None):
     """qsa_select_step from host (CPU, ideally pinned) tensors. dev_buffers =
-    (q32_dev, q16_dev, kb_dev, scores_dev, ids_dev) CUDA tensors. Enqueued on
+    (q32_dev, q16_dev or None, kb_dev, scores_dev, ids_dev) CUDA tensors. Enqueued on
     `stream` (default: current stream); synchronize before reading outputs."""
     torch = _torch()
     q32_dev, q16_dev, kb_dev, scores_dev, ids_dev = dev_buffers
@@ -255,7 +268,8 @@ def qsa_select_step_host(q32_host, kb_host, n_kv: int, k: int, block: int, score
     with torch.cuda.device(q32_dev.device):
         _check(lib.qsa_select_step_host(
             _ptr(q32_host), _ptr(kb_host), nq, H, D, n_kv, block, k, _ptr(scores_host),
-            _ptr(ids_host), _ptr(q32_dev), _ptr(q16_dev), _ptr(kb_dev), _ptr(scores_dev),
+            _ptr(ids_host), _ptr(q32_dev), _ptr(q16_dev) if q16_dev is not None else None,
+            _ptr(kb_dev), _ptr(scores_dev),
             _ptr(ids_dev), ctypes.c_void_p(stream.cuda_stream)), "qsa_select_step_host")
 
 

@@ -1,0 +1,532 @@
+// fused.cu - the whole selection step in one launch: (fp32 -> fp16 query
+// conversion,) tensor-core block scores with the fused ReLU / head-sum
+// epilogue, the fp32 tail block with the +1e9 dead-tail rule, and the exact
+// top-k select (Strata pull request 228, part 1: the block scorer and the
+// "qsa select" phase of scores + selection + fp16 conversion; pull request
+// 856, "What": the shared tail kernel and the dead-tail rule).
+//
+// Work decomposition. Queries are cut into groups of Qg queries (bn = Qg*H
+// TMEM columns). One thread-block cluster of 8 CTAs owns a group: CTA rank r
+// scores the 128-block tiles r, r+8, r+16, ... of that group, so the eight
+// CTAs together cover every KV block once while the group's query tile is
+// shared by all eight. After a cluster barrier (release/acquire) every score
+// of the group is visible, and CTA r selects the group's rows r, r+8, ....
+//
+// Roles inside a CTA (288 threads):
+//   warp 8      TMA producer and tcgen05.mma issuer (one lane), TMEM owner;
+//               two shared-memory stages for Kb tiles and two TMEM
+//               accumulators, so tile t+1 is multiplied while tile t drains;
+//   warps 0-7   the fp32 -> fp16 query conversion; then (warps 0-3 of the
+//               tail-owner CTA) the tail block while the tiles load; then the
+//               epilogue: warp w reads TMEM lane quarter w % 4 (one KV block
+//               per thread) and half w / 4 of the columns, applies ReLU, sums
+//               the H adjacent columns of each query in registers and stores
+//               the scores (a warp writes 32 consecutive blocks); after the
+//               cluster barrier, the select, one row at a time.
+// When the rows a CTA selects fit in its shared memory next to the operand
+// tiles ("DSMEM mode"), every producer of a score (epilogue or tail thread,
+// on any CTA of the cluster) also stores the score's order-preserving key
+// into the selecting CTA's key array over distributed shared memory
+// (st.shared::cluster), so the select does not read the row back from
+// global memory; otherwise it reads the row after the barrier.
+// fp32 queries are loaded by all threads, rounded to fp16 (cvt.rn) and
+// written straight into the 128-byte-swizzled operand layout; fp16 queries
+// arrive by TMA. Every wait is bounded; a CTA that gives up still reaches the
+// cluster barriers, so the cluster never hangs on them.
+#include <algorithm>
+#include <cstring>
+
+#include "qsa_device.cuh"
+#include "qsa_internal.h"
+#include "select_row.cuh"
+
+namespace qsa {
+
+constexpr int kWork = 256;         // warps 0..7: query conversion, tail, epilogue, select
+constexpr int kProducerWarp = 8;   // warp 8: TMA + tcgen05.mma issue, TMEM owner
+constexpr int kFThreads = kWork + 32;
+constexpr int kCluster = 8;
+constexpr int kFTileM = 128;
+constexpr int kFRowBytes = 128;
+constexpr int kFKAtom = 64;
+
+struct FusedArgs {
+  const float* q32;     // fp32 queries [nq,H,D], or nullptr when q arrives as fp16
+  const __half* q16in;  // fp16 queries [nq,H,D] (fp16 input only)
+  __half* q16out;       // optional fp16 copy of the converted queries (fp32 input only)
+  const __half* kb;     // [nb, D]
+  float* scores;        // [nq, nb]
+  int32_t* ids;         // [nq, k]
+  int32_t nq, D, nb, n_full, has_tail, k;
+  int32_t bn, qg, m_tiles, n_chunks, k_steps;
+  uint32_t tmem_cols;
+  uint32_t sel_bytes;   // shared bytes of one select group (cand + sel, plus keys +
+                        // hist in global mode)
+  int32_t dsmem;        // 1: keys and first-digit histograms arrive over DSMEM
+  uint32_t row_bytes;   // DSMEM mode: bytes of one row's keys + histogram
+  uint32_t rows_off;    // DSMEM mode: offset of the row regions in dynamic smem
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_release_acquire() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Sends one score's key to keys[b] of the row's region in the CTA that
+// selects the row (rank ql % 8, row slot ql / 8). A plain remote store: the
+// owner builds the row's histogram itself, since remote atomics are slow.
+__device__ __forceinline__ void send_key(uint32_t rows_base, uint32_t row_bytes, int ql, int b,
+                                         float score) {
+  const uint32_t local = rows_base + static_cast<uint32_t>(ql >> 3) * row_bytes;
+  const uint32_t remote = cluster_map(local, static_cast<uint32_t>(ql & 7));
+  st_cluster_u32(remote + static_cast<uint32_t>(b) * 4u, score_key(score));
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Byte offset of fp16 element (row, i) in a K-major tile of `rows` rows stored
+// as 64-column chunks of 128-byte rows with the 128-byte swizzle (16-byte
+// unit u of row r lives at unit u ^ (r & 7)).
+__device__ __forceinline__ uint32_t sw128_offset(int rows, int row, int i) {
+  const int chunk = i >> 6;
+  const int unit = (i & 63) >> 3;
+  return static_cast<uint32_t>(chunk * rows * kFRowBytes + row * kFRowBytes +
+                               ((unit ^ (row & 7)) << 4) + ((i & 7) << 1));
+}
+
+template <int H, bool kF32Q>
+__global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
+    fused_step_kernel(const __grid_constant__ CUtensorMap tm_kb,
+                      const __grid_constant__ CUtensorMap tm_q, const FusedArgs a) {
+  static_assert(32 % H == 0, "a 32-column TMEM load must hold whole queries");
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_full[2], bar_empty[2], bar_acc_full[2], bar_acc_empty[2], bar_q;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int failed;
+  __shared__ float tail_acc[256];
+  __shared__ SelectShared sel_sh;
+
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint8_t* sQ = smem;                                             // n_chunks x bn rows x 128 B
+  uint8_t* sKB = sQ + a.n_chunks * a.bn * kFRowBytes;              // 2 stages
+  const int stage_bytes = a.n_chunks * kFTileM * kFRowBytes;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = static_cast<int>(cluster_rank());
+  const int group = blockIdx.x / kCluster;
+  const int q0 = group * a.qg;                 // first query of the group
+  const int col0 = q0 * H;                     // first row of the [nq*H, D] query view
+  const int qh_rows = min(a.bn, (a.nq - q0) * H);
+  const int n_local = a.m_tiles > rank ? (a.m_tiles - rank + kCluster - 1) / kCluster : 0;
+  const bool tail_owner = a.has_tail && rank == kCluster - 1;
+  const bool need_q = n_local > 0 || tail_owner || (kF32Q && a.q16out != nullptr && rank == 0);
+  const int rows_here = a.qg > rank ? (a.qg - rank + kCluster - 1) / kCluster : 0;
+  const uint32_t rows_base = smem_u32(smem + a.rows_off);
+  const bool producer_warp = warp == kProducerWarp;
+
+  if (tid == kProducerWarp * 32) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+      mbar_init(&bar_acc_full[s], 1);
+      mbar_init(&bar_acc_empty[s], kWork);
+    }
+    mbar_init(&bar_q, 1);
+    failed = 0;
+    fence_mbarrier_init();
+    if (n_local > 0) tma_prefetch_desc(&tm_kb);
+    if (!kF32Q && need_q) {
+      tma_prefetch_desc(&tm_q);
+      mbar_arrive_expect_tx(&bar_q, static_cast<uint32_t>(a.n_chunks * a.bn * kFRowBytes));
+      for (int c = 0; c < a.n_chunks; ++c)
+        tma_load_2d(sQ + c * a.bn * kFRowBytes, &tm_q, c * kFKAtom, col0, &bar_q);
+    }
+    for (int t = 0; t < 2 && t < n_local; ++t) {
+      const int m = rank + t * kCluster;
+      mbar_arrive_expect_tx(&bar_full[t], static_cast<uint32_t>(stage_bytes));
+      for (int c = 0; c < a.n_chunks; ++c)
+        tma_load_2d(sKB + t * stage_bytes + c * kFTileM * kFRowBytes, &tm_kb, c * kFKAtom,
+                    m * kFTileM, &bar_full[t]);
+    }
+  }
+  // DSMEM mode: peers store into this CTA's shared memory only after every
+  // CTA of the cluster has started (this arrive, the wait below).
+  if (a.dsmem) cluster_arrive_release();
+  __syncwarp();
+  if (producer_warp) {
+    if (n_local > 0) {
+      tmem_alloc(&tmem_slot, a.tmem_cols);
+      tmem_relinquish();
+    }
+  } else if (kF32Q && need_q) {
+    // fp32 queries -> fp16 (round to nearest even) -> swizzled operand tile,
+    // by the kWork threads. Rows past the last query and columns past D are 0.
+    const int f4_per_row = a.n_chunks * (kFKAtom / 4);
+    const int total = a.bn * f4_per_row;
+    for (int base = 0; base < total; base += 8 * kWork) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int f = base + j * kWork + tid;
+        const int row = f / f4_per_row;
+        const int i = (f - row * f4_per_row) * 4;
+        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (f < total && row < qh_rows && i < a.D)
+          v[j] = __ldg(reinterpret_cast<const float4*>(a.q32 + static_cast<int64_t>(col0 + row) * a.D + i));
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int f = base + j * kWork + tid;
+        if (f < total) {
+          const int row = f / f4_per_row;
+          const int i = (f - row * f4_per_row) * 4;
+          const __half2 h01 = __floats2half2_rn(v[j].x, v[j].y);
+          const __half2 h23 = __floats2half2_rn(v[j].z, v[j].w);
+          uint2 pk;
+          pk.x = *reinterpret_cast<const uint32_t*>(&h01);
+          pk.y = *reinterpret_cast<const uint32_t*>(&h23);
+          *reinterpret_cast<uint2*>(sQ + sw128_offset(a.bn, row, i)) = pk;
+          if (a.q16out != nullptr && rank == 0 && row < qh_rows && i < a.D)
+            *reinterpret_cast<uint2*>(a.q16out + static_cast<int64_t>(col0 + row) * a.D + i) = pk;
+        }
+      }
+    }
+    fence_proxy_async_smem();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = tmem_slot;
+  if (a.dsmem) cluster_wait_acquire();
+
+  if (producer_warp) {
+    // ---------------------------------------------------- producer / MMA
+    if (lane == 0 && n_local > 0) {
+      const uint32_t idesc = idesc_f16_f32(kFTileM, a.bn);
+      bool ok = kF32Q ? true : mbar_wait_bounded(&bar_q, 0, a.timeout_ns);
+      for (int t = 0; t < n_local && ok; ++t) {
+        const int s = t & 1;
+        const uint32_t use = static_cast<uint32_t>(t >> 1);
+        if (!mbar_wait_bounded(&bar_full[s], use & 1u, a.timeout_ns)) { ok = false; break; }
+        if (t >= 2 && !mbar_wait_bounded(&bar_acc_empty[s], (use - 1) & 1u, a.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(s * a.bn);
+        const uint32_t a_base = smem_u32(sKB + s * stage_bytes);
+        const uint32_t b_base = smem_u32(sQ);
+        for (int step = 0; step < a.k_steps; ++step) {
+          const int c = step >> 2, kk = step & 3;
+          mma_f16_ss(d_tmem, smem_desc_k_sw128(a_base + c * kFTileM * kFRowBytes + kk * 32),
+                     smem_desc_k_sw128(b_base + c * a.bn * kFRowBytes + kk * 32), idesc,
+                     step > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar_acc_full[s]);
+        mma_commit(&bar_empty[s]);
+        if (t + 2 < n_local) {
+          if (!mbar_wait_bounded(&bar_empty[s], use & 1u, a.timeout_ns)) { ok = false; break; }
+          const int m = rank + (t + 2) * kCluster;
+          mbar_arrive_expect_tx(&bar_full[s], static_cast<uint32_t>(stage_bytes));
+          for (int c = 0; c < a.n_chunks; ++c)
+            tma_load_2d(sKB + s * stage_bytes + c * kFTileM * kFRowBytes, &tm_kb, c * kFKAtom,
+                        m * kFTileM, &bar_full[s]);
+        }
+      }
+      if (!ok) {
+        failed = 1;
+        atomicOr(a.status, kErrScoreLoadTimeout);
+        // Complete both accumulators' "full" barriers so the epilogue does not
+        // wait out its own bound, then drain loads still in flight.
+        mma_commit(&bar_acc_full[0]);
+        mma_commit(&bar_acc_full[1]);
+        for (int s = 0; s < 2 && s < n_local; ++s) mbar_wait_bounded(&bar_full[s], 0, a.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ tail block (warps 0..3 of the owner)
+    if (tail_owner && warp < 4) {
+      if (!kF32Q && !mbar_wait_bounded(&bar_q, 0, a.timeout_ns)) {
+        failed = 1;
+        atomicOr(a.status, kErrScoreLoadTimeout);
+      }
+      const int pairs = qh_rows;
+      const __half* krow = a.kb + static_cast<int64_t>(a.nb - 1) * a.D;
+      for (int p = tid; p < pairs; p += 128) {
+        float acc = 0.0f;
+        for (int i = 0; i < a.D; i += 8) {
+          const uint4 kv = __ldg(reinterpret_cast<const uint4*>(krow + i));
+          const uint4 qv = *reinterpret_cast<const uint4*>(sQ + sw128_offset(a.bn, p, i));
+          const __half* kh = reinterpret_cast<const __half*>(&kv);
+          const __half* qh = reinterpret_cast<const __half*>(&qv);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            acc = __fadd_rn(acc, __fmul_rn(__half2float(qh[j]), __half2float(kh[j])));
+        }
+        tail_acc[p] = acc;
+      }
+      asm volatile("bar.sync 3, 128;" ::: "memory");
+      for (int ql = tid; ql * H < pairs; ql += 128) {
+        float s = 0.0f;
+#pragma unroll
+        for (int h = 0; h < H; ++h) s = __fadd_rn(s, fmaxf(tail_acc[ql * H + h], 0.0f));
+        const float score = __fadd_rn(s, 1.0e9f);
+        a.scores[static_cast<int64_t>(q0 + ql) * a.nb + (a.nb - 1)] = score;
+        if (a.dsmem) send_key(rows_base, a.row_bytes, ql, a.nb - 1, score);
+      }
+    }
+    // ---------------------------------------- epilogue (warps 0..7)
+    // Warp w reads TMEM lane quarter w % 4 (one KV block per thread) and the
+    // half w / 4 of the tile's columns.
+    const int quarter = warp & 3;
+    const int half_cols = a.bn >> 1;
+    const int c_begin = (warp >> 2) * half_cols;
+    for (int t = 0; t < n_local; ++t) {
+      const int s = t & 1;
+      const uint32_t use = static_cast<uint32_t>(t >> 1);
+      if (!mbar_wait_bounded(&bar_acc_full[s], use & 1u, a.timeout_ns)) {
+        failed = 1;
+        if (lane == 0) atomicOr(a.status, kErrScoreMmaTimeout);
+        break;
+      }
+      tc_fence_after_sync();
+      if (failed) break;
+      const int b = (rank + t * kCluster) * kFTileM + quarter * 32 + lane;
+      const bool b_ok = b < a.n_full;
+      float* out = a.scores + b;
+      const uint32_t taddr =
+          tmem_base + static_cast<uint32_t>(s * a.bn) + (static_cast<uint32_t>(quarter * 32) << 16);
+      constexpr int kQPerLoad = 32 / H;
+      for (int c0 = c_begin; c0 < c_begin + half_cols; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32cols(taddr + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < kQPerLoad; ++j) {
+          float sc = 0.0f;
+#pragma unroll
+          for (int h = 0; h < H; ++h) sc = __fadd_rn(sc, fmaxf(__uint_as_float(r[j * H + h]), 0.0f));
+          const int ql = c0 / H + j;
+          if (b_ok && q0 + ql < a.nq) {
+            out[static_cast<int64_t>(q0 + ql) * a.nb] = sc;
+            if (a.dsmem) send_key(rows_base, a.row_bytes, ql, b, sc);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&bar_acc_empty[s]);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (n_local > 0 && producer_warp) tmem_dealloc(tmem_base, a.tmem_cols);
+
+  // Every score (and, in DSMEM mode, every key) of the group is written and
+  // visible after this barrier.
+  cluster_sync_release_acquire();
+  if (producer_warp) return;  // the select runs on the kWork threads
+
+  // ---------------------------------------------------------- select
+  // One row at a time with the kWork threads. hist / cand / sel (and, for
+  // long rows, keys) reuse the dead operand tiles.
+  uint64_t* cand = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* sel = cand + kSelCandMax;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sel + a.k);
+  uint32_t* keys = hist + kSelHistBins;
+  for (int r = 0; r < rows_here; ++r) {
+    const int qi = q0 + rank + r * kCluster;
+    if (qi >= a.nq) break;
+    int32_t* out = a.ids + static_cast<int64_t>(qi) * a.k;
+    const float* row = a.scores + static_cast<int64_t>(qi) * a.nb;
+    const uint32_t* rk = reinterpret_cast<const uint32_t*>(smem + a.rows_off + r * a.row_bytes);
+    if (a.nb <= 8 * kWork) {
+      uint32_t key[8];
+      if (a.dsmem) load_keys_smem<kWork, 8>(rk, a.nb, key, hist, tid, 1);
+      else load_keys_global<kWork, 8>(row, a.nb, key, hist, tid, 1);
+      select_row_regs<kWork, 8>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1);
+    } else if (a.nb <= 16 * kWork) {
+      uint32_t key[16];
+      if (a.dsmem) load_keys_smem<kWork, 16>(rk, a.nb, key, hist, tid, 1);
+      else load_keys_global<kWork, 16>(row, a.nb, key, hist, tid, 1);
+      select_row_regs<kWork, 16>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1);
+    } else {
+      select_row_smem<kWork, true>(row, a.nb, a.k, out, keys, hist, cand, sel, sel_sh, tid, 1);
+    }
+    group_sync<kWork>(1);
+  }
+}
+
+// ------------------------------------------------------------------ host
+namespace {
+
+template <int H, bool F>
+const void* fused_ptr() {
+  return reinterpret_cast<const void*>(&fused_step_kernel<H, F>);
+}
+
+const void* fused_kernel_for(int H, bool f32q) {
+  switch (H) {
+    case 1: return f32q ? fused_ptr<1, true>() : fused_ptr<1, false>();
+    case 2: return f32q ? fused_ptr<2, true>() : fused_ptr<2, false>();
+    case 4: return f32q ? fused_ptr<4, true>() : fused_ptr<4, false>();
+    case 8: return f32q ? fused_ptr<8, true>() : fused_ptr<8, false>();
+    case 16: return f32q ? fused_ptr<16, true>() : fused_ptr<16, false>();
+    case 32: return f32q ? fused_ptr<32, true>() : fused_ptr<32, false>();
+    default: return nullptr;
+  }
+}
+
+bool encode_f16_2d(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows,
+                   uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int g_fused_static_smem = 0;
+
+cudaError_t init_fused_kernels(const DeviceInfo& dev) {
+  for (int H : {1, 2, 4, 8, 16, 32})
+    for (bool f : {false, true}) {
+      cudaFuncAttributes fa;
+      cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel_for(H, f));
+      if (e != cudaSuccess) return e;
+      g_fused_static_smem = std::max(g_fused_static_smem, static_cast<int>(fa.sharedSizeBytes));
+      e = cudaFuncSetAttribute(fused_kernel_for(H, f), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dev.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
+      if (e != cudaSuccess) return e;
+    }
+  return cudaSuccess;
+}
+
+cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStream_t stream) {
+  if (p.nq <= 0) return cudaSuccess;
+  // Columns per group: 64 unless that would need more than about two waves
+  // of 8-CTA clusters, then 128.
+  int bn = 64;
+  if (bn < p.H) bn = p.H;
+  {
+    const int64_t groups64 = (p.nq + (64 / std::min(64, p.H)) - 1) / (64 / std::min(64, p.H));
+    if (groups64 * kCluster > 4LL * dev.sm_count) bn = 128;
+  }
+  const int qg = bn / p.H;
+  const int64_t groups = (p.nq + qg - 1) / qg;
+  if (groups * kCluster > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  FusedArgs a;
+  a.q32 = p.q32;
+  a.q16in = reinterpret_cast<const __half*>(p.q16);
+  a.q16out = reinterpret_cast<__half*>(p.q16out);
+  a.kb = reinterpret_cast<const __half*>(p.kb);
+  a.scores = p.scores;
+  a.ids = p.ids;
+  a.nq = p.nq;
+  a.D = p.D;
+  a.nb = static_cast<int32_t>(p.nb);
+  a.n_full = static_cast<int32_t>(p.n_full);
+  a.has_tail = p.has_tail ? 1 : 0;
+  a.k = p.k;
+  a.bn = bn;
+  a.qg = qg;
+  a.m_tiles = static_cast<int32_t>((p.n_full + kFTileM - 1) / kFTileM);
+  a.n_chunks = (p.D + kFKAtom - 1) / kFKAtom;
+  a.k_steps = p.D / 16;
+  a.tmem_cols = 2u * static_cast<uint32_t>(bn) <= 32u ? 32u : 2u * static_cast<uint32_t>(bn);
+  a.status = dev.status_word;
+  a.timeout_ns = kWaitTimeoutNs;
+  const int rows_per_cta = (qg + kCluster - 1) / kCluster;
+  const size_t operand_bytes = static_cast<size_t>(a.n_chunks) * (bn + 2 * kFTileM) * kFRowBytes;
+  const size_t budget = static_cast<size_t>(dev.max_smem_optin) - g_fused_static_smem - 1024;
+  // Select scratch in the operand region after the epilogue: cand, sel,
+  // hist, and the keys of a long row (> 4096 blocks) read from global.
+  size_t sel_bytes = (static_cast<size_t>(kSelCandMax) + p.k) * sizeof(uint64_t) +
+                     kSelHistBins * sizeof(uint32_t);
+  if (p.nb > 16 * kWork) sel_bytes += static_cast<size_t>(p.nb) * sizeof(uint32_t);
+  // DSMEM mode when the keys of the rows this CTA selects fit beside the
+  // operand tiles (register path only: nb <= 4096).
+  const size_t row_bytes = static_cast<size_t>((a.nb + 3) & ~3) * sizeof(uint32_t);
+  const size_t rows_off = (std::max(operand_bytes, sel_bytes) + 1023) & ~static_cast<size_t>(1023);
+  a.dsmem = (p.nb <= 16 * kWork && rows_off + rows_per_cta * row_bytes <= budget) ? 1 : 0;
+  a.sel_bytes = static_cast<uint32_t>(sel_bytes);
+  a.row_bytes = static_cast<uint32_t>(row_bytes);
+  a.rows_off = static_cast<uint32_t>(rows_off);
+  size_t smem = a.dsmem ? rows_off + rows_per_cta * row_bytes : std::max(operand_bytes, sel_bytes);
+  smem += 1024;  // alignment slack
+  if (smem + g_fused_static_smem > static_cast<size_t>(dev.max_smem_optin)) return cudaErrorInvalidValue;
+
+  CUtensorMap tm_kb, tm_q;
+  memset(&tm_kb, 0, sizeof(tm_kb));
+  memset(&tm_q, 0, sizeof(tm_q));
+  if (p.n_full > 0 && !encode_f16_2d(&tm_kb, p.kb, p.D, p.n_full, kFKAtom, kFTileM))
+    return cudaErrorInvalidValue;
+  if (p.q32 == nullptr &&
+      !encode_f16_2d(&tm_q, p.q16, p.D, static_cast<uint64_t>(p.nq) * p.H, kFKAtom, bn))
+    return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(groups * kCluster));
+  const bool f32q = p.q32 != nullptr;
+#define QSA_FUSED_LAUNCH(HH)                                                               \
+  case HH:                                                                                 \
+    if (f32q)                                                                              \
+      fused_step_kernel<HH, true><<<grid, kFThreads, smem, stream>>>(tm_kb, tm_q, a);      \
+    else                                                                                   \
+      fused_step_kernel<HH, false><<<grid, kFThreads, smem, stream>>>(tm_kb, tm_q, a);     \
+    break;
+  switch (p.H) {
+    QSA_FUSED_LAUNCH(1)
+    QSA_FUSED_LAUNCH(2)
+    QSA_FUSED_LAUNCH(4)
+    QSA_FUSED_LAUNCH(8)
+    QSA_FUSED_LAUNCH(16)
+    QSA_FUSED_LAUNCH(32)
+    default: return cudaErrorInvalidValue;
+  }
+#undef QSA_FUSED_LAUNCH
+  return cudaGetLastError();
+}
+
+}  // namespace qsa

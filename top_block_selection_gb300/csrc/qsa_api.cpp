@@ -1,7 +1,7 @@
 // qsa_api.cpp - the C ABI (include/qsa.h): host-side validation, block
 // partition, and stream-ordered launches. Arguments are checked before any
 // CUDA call, so a bad call returns a status without touching the device.
-#include "../../include/qsa.h"
+#include "qsa.h"
 
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -20,11 +20,20 @@ bool supported_heads(int32_t H) {
 
 cudaStream_t as_cuda(qsa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
+thread_local const char* t_last_cuda_error = "no error";
+
+qsa_status cuda_fail(cudaError_t e) {
+  t_last_cuda_error = cudaGetErrorString(e);
+  return QSA_ERR_CUDA;
+}
+
+qsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QSA_OK : cuda_fail(e); }
+
 // Returns the current device's info, or an error status.
 qsa_status device_or_error(const DeviceInfo** out) {
   cudaError_t e = cudaSuccess;
   const DeviceInfo* d = qsa::current_device(&e);
-  if (!d) return QSA_ERR_CUDA;
+  if (!d) return cuda_fail(e);
   if (!d->supported) return QSA_ERR_UNSUPPORTED_ARCH;
   *out = d;
   return QSA_OK;
@@ -66,7 +75,7 @@ qsa_status run_scores(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t
                       cudaStream_t stream) {
   if (nq == 0 || g.nb == 0) return QSA_OK;
   qsa::ScoreProblem p{q, kb, scores, nq, H, D, g.nb, g.n_full, g.has_tail};
-  return qsa::launch_scores(p, dev, stream) == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
+  return from_cuda(qsa::launch_scores(p, dev, stream));
 }
 
 }  // namespace
@@ -74,6 +83,8 @@ qsa_status run_scores(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t
 extern "C" {
 
 int qsa_abi_version(void) { return QSA_ABI_VERSION; }
+
+const char* qsa_last_cuda_error(void) { return t_last_cuda_error; }
 
 const char* qsa_status_str(qsa_status s) {
   switch (s) {
@@ -107,8 +118,7 @@ qsa_status qsa_f32_to_f16(const float* src, uint16_t* dst, int64_t n, qsa_stream
   const DeviceInfo* dev = nullptr;
   qsa_status st = device_or_error(&dev);
   if (st != QSA_OK) return st;
-  return qsa::launch_convert(src, dst, n, *dev, as_cuda(stream)) == cudaSuccess ? QSA_OK
-                                                                                 : QSA_ERR_CUDA;
+  return from_cuda(qsa::launch_convert(src, dst, n, *dev, as_cuda(stream)));
 }
 
 qsa_status qsa_block_scores(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H,
@@ -128,9 +138,7 @@ qsa_status qsa_select(const float* scores, int32_t nq, int32_t nb, int32_t k, in
   if (st != QSA_OK || nq == 0) return st;
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
-  return qsa::launch_select(scores, nq, nb, k, ids, *dev, as_cuda(stream)) == cudaSuccess
-             ? QSA_OK
-             : QSA_ERR_CUDA;
+  return from_cuda(qsa::launch_select(scores, nq, nb, k, ids, *dev, as_cuda(stream)));
 }
 
 qsa_status qsa_score_select(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H,
@@ -141,40 +149,29 @@ qsa_status qsa_score_select(const uint16_t* q, const uint16_t* kb, int32_t nq, i
   if (st != QSA_OK) return st;
   if ((st = check_select(scores, nq, g.nb, k, ids)) != QSA_OK) return st;
   if (nq == 0) return QSA_OK;
+  if (g.nb > 0 && (!q || !kb)) return QSA_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
-  cudaStream_t s = as_cuda(stream);
-  if ((st = run_scores(q, kb, nq, H, D, g, scores, *dev, s)) != QSA_OK) return st;
-  return qsa::launch_select(scores, nq, static_cast<int32_t>(g.nb), k, ids, *dev, s) ==
-                 cudaSuccess
-             ? QSA_OK
-             : QSA_ERR_CUDA;
+  qsa::FusedProblem p{nullptr, q, nullptr, kb, scores, ids, nq, H, D, g.nb, g.n_full, g.has_tail, k};
+  return from_cuda(qsa::launch_fused(p, *dev, as_cuda(stream)));
 }
 
 qsa_status qsa_select_step(const float* q32, uint16_t* q16, const uint16_t* kb, int32_t nq,
                            int32_t H, int32_t D, int64_t n_kv, int32_t block, int32_t k,
                            float* scores, int32_t* ids, qsa_stream_t stream) {
   Geometry g;
-  qsa_status st = check_scores(q16, kb, nq, H, D, n_kv, block, scores, &g);
+  // q16 is optional here; the scoring checks see the (aligned) q32 in its place.
+  qsa_status st = check_scores(reinterpret_cast<const uint16_t*>(q32), kb, nq, H, D, n_kv, block,
+                               scores, &g);
   if (st != QSA_OK) return st;
   if ((st = check_select(scores, nq, g.nb, k, ids)) != QSA_OK) return st;
   if (nq == 0) return QSA_OK;
-  if (!q32 || !q16) return QSA_ERR_INVALID_ARG;
-  if (!aligned(q32, 4) || !aligned(q16, 16)) return QSA_ERR_MISALIGNED;
+  if (!q32) return QSA_ERR_INVALID_ARG;
+  if (!aligned(q32, 16) || !aligned(q16, 16)) return QSA_ERR_MISALIGNED;
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
-  cudaStream_t s = as_cuda(stream);
-  const int64_t n = static_cast<int64_t>(nq) * H * D;
-  if (qsa::launch_convert(q32, q16, n, *dev, s) != cudaSuccess) return QSA_ERR_CUDA;
-  if (g.nb == 0) {
-    return qsa::launch_select(scores, nq, 0, k, ids, *dev, s) == cudaSuccess ? QSA_OK
-                                                                             : QSA_ERR_CUDA;
-  }
-  if ((st = run_scores(q16, kb, nq, H, D, g, scores, *dev, s)) != QSA_OK) return st;
-  return qsa::launch_select(scores, nq, static_cast<int32_t>(g.nb), k, ids, *dev, s) ==
-                 cudaSuccess
-             ? QSA_OK
-             : QSA_ERR_CUDA;
+  qsa::FusedProblem p{q32, nullptr, q16, kb, scores, ids, nq, H, D, g.nb, g.n_full, g.has_tail, k};
+  return from_cuda(qsa::launch_fused(p, *dev, as_cuda(stream)));
 }
 
 qsa_status qsa_select_step_host(const float* q32_host, const uint16_t* kb_host, int32_t nq,
@@ -183,11 +180,12 @@ qsa_status qsa_select_step_host(const float* q32_host, const uint16_t* kb_host, 
                                 uint16_t* q16_dev, uint16_t* kb_dev, float* scores_dev,
                                 int32_t* ids_dev, qsa_stream_t stream) {
   Geometry g;
-  qsa_status st = check_scores(q16_dev, kb_dev, nq, H, D, n_kv, block, scores_dev, &g);
+  qsa_status st = check_scores(reinterpret_cast<const uint16_t*>(q32_dev), kb_dev, nq, H, D, n_kv,
+                               block, scores_dev, &g);
   if (st != QSA_OK) return st;
   if ((st = check_select(scores_dev, nq, g.nb, k, ids_dev)) != QSA_OK) return st;
   if (nq == 0) return QSA_OK;
-  if (!q32_host || !ids_host || !q32_dev || !q16_dev || !ids_dev) return QSA_ERR_INVALID_ARG;
+  if (!q32_host || !ids_host || !q32_dev || !ids_dev) return QSA_ERR_INVALID_ARG;
   if (g.nb > 0 && (!kb_host || !scores_host)) return QSA_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
@@ -197,18 +195,18 @@ qsa_status qsa_select_step_host(const float* q32_host, const uint16_t* kb_host, 
   const size_t s_bytes = static_cast<size_t>(nq) * g.nb * sizeof(float);
   const size_t id_bytes = static_cast<size_t>(nq) * k * sizeof(int32_t);
   if (cudaMemcpyAsync(q32_dev, q32_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return QSA_ERR_CUDA;
+    return cuda_fail(cudaGetLastError());
   if (kb_bytes &&
       cudaMemcpyAsync(kb_dev, kb_host, kb_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return QSA_ERR_CUDA;
+    return cuda_fail(cudaGetLastError());
   st = qsa_select_step(q32_dev, q16_dev, kb_dev, nq, H, D, n_kv, block, k, scores_dev, ids_dev,
                        stream);
   if (st != QSA_OK) return st;
   if (s_bytes &&
       cudaMemcpyAsync(scores_host, scores_dev, s_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return QSA_ERR_CUDA;
+    return cuda_fail(cudaGetLastError());
   if (cudaMemcpyAsync(ids_host, ids_dev, id_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return QSA_ERR_CUDA;
+    return cuda_fail(cudaGetLastError());
   return QSA_OK;
 }
 
@@ -216,15 +214,16 @@ qsa_status qsa_device_status(int clear, uint32_t* bits, qsa_stream_t stream) {
   const DeviceInfo* dev = nullptr;
   qsa_status st = device_or_error(&dev);
   if (st != QSA_OK) return st;
-  if (cudaStreamSynchronize(as_cuda(stream)) != cudaSuccess) return QSA_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(as_cuda(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
   uint32_t v = 0;
-  if (cudaMemcpy(&v, dev->status_word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return QSA_ERR_CUDA;
+  if ((e = cudaMemcpy(&v, dev->status_word, sizeof(v), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e);
   if (bits) *bits = v;
   if (v != 0 && clear) {
-    if (cudaMemset(dev->status_word, 0, sizeof(uint32_t)) != cudaSuccess ||
-        cudaDeviceSynchronize() != cudaSuccess)
-      return QSA_ERR_CUDA;
+    if ((e = cudaMemset(dev->status_word, 0, sizeof(uint32_t))) != cudaSuccess ||
+        (e = cudaDeviceSynchronize()) != cudaSuccess)
+      return cuda_fail(e);
   }
   return v == 0 ? QSA_OK : QSA_ERR_TIMEOUT;
 }

@@ -49,6 +49,24 @@ struct ScoreProblem {
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStream_t stream);
 
+// The fused step: optional fp32->fp16 conversion of q, block scores (full
+// blocks and tail) and the top-k select in one cluster launch. Exactly one of
+// q32 / q16 is non-null; q16out (fp32 input only) may be null.
+struct FusedProblem {
+  const float* q32;
+  const uint16_t* q16;
+  uint16_t* q16out;
+  const uint16_t* kb;
+  float* scores;
+  int32_t* ids;
+  int32_t nq, H, D;
+  int64_t nb, n_full;
+  bool has_tail;
+  int32_t k;
+};
+cudaError_t init_fused_kernels(const DeviceInfo& dev);
+cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStream_t stream);
+
 cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k, int32_t* ids,
                           const DeviceInfo& dev, cudaStream_t stream);
 

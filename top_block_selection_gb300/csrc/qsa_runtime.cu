@@ -43,7 +43,8 @@ const DeviceInfo* current_device(cudaError_t* err) {
       return nullptr;
     }
     d.status_word = static_cast<uint32_t*>(p);
-    if ((e = init_score_kernels(d)) != cudaSuccess || (e = init_select_kernels(d)) != cudaSuccess) {
+    if ((e = init_score_kernels(d)) != cudaSuccess || (e = init_select_kernels(d)) != cudaSuccess ||
+        (e = init_fused_kernels(d)) != cudaSuccess) {
       *err = e;
       return nullptr;
     }

@@ -249,11 +249,12 @@ int choose_bn(int64_t m_tiles, int64_t cols, int sm_count) {
 }  // namespace
 
 cudaError_t init_score_kernels(const DeviceInfo& dev) {
-  const size_t max_smem = static_cast<size_t>(dev.max_smem_optin);
   for (int H : {1, 2, 4, 8, 16, 32}) {
-    cudaError_t e = cudaFuncSetAttribute(score_kernel_for(H),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(max_smem));
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, score_kernel_for(H));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(score_kernel_for(H), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dev.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -1,0 +1,453 @@
+// select_row.cuh - exact top-k of one score row by a group of T threads (T a
+// multiple of 32, whole warps, synchronised by one named barrier).
+//
+// Order (Strata pull request 228 part 1 and pull request 856 "Arithmetic
+// contract and parity": top-k over the block scores, with a block-index
+// tie-break): descending score; equal scores -> smaller block index first;
+// -0.0 == +0.0; ids past nb are -1.
+//
+// Scores are compared as order-preserving uint32 keys (score_key). The search
+// is a radix select on the keys, most significant digit first:
+//   * the first digit is fixed, the top 11 key bits (sign, exponent, two
+//     mantissa bits: quarter-octave bins), so its histogram can be built
+//     while the row is loaded, or by whoever produces the scores;
+//   * one suffix scan over the bins finds the digit holding the k-th largest
+//     key; every key in a higher bin is a winner;
+//   * the search stops as soon as (a) the keys still needed fill the boundary
+//     bin exactly, (b) the boundary bin holds at most kSelCandMax keys, which
+//     are then ranked by (key, index) directly, or (c) the key is resolved to
+//     all 32 bits, when the tied keys with the smallest indices are taken in
+//     index order; otherwise the next 8 bits of the boundary bin's keys are
+//     histogrammed (a pass over a handful of keys is cheaper than ranking a
+//     large bin pairwise);
+//   * winners and candidates are gathered by per-thread counts and one group
+//     scan (no atomics), and every rank (candidate or final output slot) is
+//     computed by several threads per element, reduced with shuffles.
+// A winner is the 64-bit key (key << 32 | ~index): all distinct, and larger
+// means earlier in the output.
+#pragma once
+
+#include "qsa_device.cuh"
+
+namespace qsa {
+
+constexpr int kSelFirstBits = 11;
+constexpr int kSelFirstShift = 32 - kSelFirstBits;
+constexpr int kSelHistBins = 1 << kSelFirstBits;
+constexpr int kSelCandMax = 32;
+
+struct SelectShared {
+  uint32_t wsum[32];
+  uint32_t digit, above, cnt;
+};
+
+__device__ __forceinline__ uint32_t lane_mask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+template <int T>
+__device__ __forceinline__ void group_sync(int bar_id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(T) : "memory");
+}
+
+__device__ __forceinline__ uint64_t win_key(uint32_t key, int idx) {
+  return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~idx);
+}
+
+// Exclusive scan of v over the group in thread order; *total gets the sum.
+// Ends with a barrier, so sh.wsum may be reused right after.
+template <int T>
+__device__ __forceinline__ uint32_t group_excl_scan(uint32_t v, uint32_t* total, SelectShared& sh,
+                                                    int gtid, int bar_id) {
+  constexpr int kWarps = T / 32;
+  const int lane = gtid & 31, gwarp = gtid >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  if (lane == 31) sh.wsum[gwarp] = incl;
+  group_sync<T>(bar_id);
+  uint32_t before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t x = sh.wsum[w];
+    before += (w < gwarp) ? x : 0u;
+    tot += x;
+  }
+  group_sync<T>(bar_id);
+  *total = tot;
+  return before + incl - v;
+}
+
+// For j < n: emit(j, #{m < n : x[m] > x[j]}). P consecutive threads share an
+// element (P a power of two <= 32 with P * n <= T where possible), each
+// comparing a strided slice, and add their counts with shuffles.
+template <int T, typename Emit>
+__device__ __forceinline__ void split_rank(const uint64_t* x, int n, int gtid, Emit emit) {
+  int P = 1;
+  while (P < 32 && 2 * P * n <= T) P <<= 1;
+  const int slots = n * P;
+  for (int base = 0; base < slots; base += T) {
+    const int t = base + gtid;
+    const int e = t / P;
+    const int sub = t & (P - 1);
+    const bool valid = t < slots;
+    const uint64_t me = valid ? x[e] : 0ull;
+    uint32_t r = 0;
+    if (valid) {
+      int m = sub;
+#pragma unroll 4
+      for (; m < n; m += P) r += x[m] > me ? 1u : 0u;
+    }
+    for (int o = 1; o < P; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
+    if (valid && sub == 0) emit(e, r);
+  }
+}
+
+// Finds the digit of the bins [0, nbins) holding the need-th largest key
+// (counting from the top bin down); writes digit, count above it and its own
+// count to sh. Thread t owns bins [nbins - (t+1)B, nbins - tB).
+template <int T>
+__device__ __forceinline__ void scan_bins(const uint32_t* hist, int nbins, uint32_t need,
+                                          SelectShared& sh, int gtid, int bar_id) {
+  const int B = nbins >= T ? nbins / T : 1;
+  const int top = nbins - gtid * B;
+  uint32_t local = 0;
+  if (top > 0) {
+    for (int j = 1; j <= B; ++j) local += hist[top - j];
+  }
+  uint32_t tot;
+  const uint32_t excl = group_excl_scan<T>(local, &tot, sh, gtid, bar_id);
+  const uint32_t incl = excl + local;
+  if (excl < need && need <= incl) {
+    uint32_t run = excl;
+    for (int j = 1; j <= B; ++j) {
+      const uint32_t c = hist[top - j];
+      if (run + c >= need) {
+        sh.digit = static_cast<uint32_t>(top - j);
+        sh.above = run;
+        sh.cnt = c;
+        break;
+      }
+      run += c;
+    }
+  }
+  group_sync<T>(bar_id);
+}
+
+// Top-k of one row, keys staged in shared memory (any nb up to the shared
+// memory budget). With kFromGlobal the row is read from `s` (ld.global.cg:
+// it may have been written by other CTAs of the same kernel) into keys[] and
+// the first-digit histogram is built here; otherwise keys[0..nb) and the
+// first-digit histogram in hist[] must already be complete.
+// Shared arrays of this group: keys[nb], hist[kSelHistBins], cand[kSelCandMax],
+// sel[min(k, nb)].
+template <int T, bool kFromGlobal>
+__device__ void select_row_smem(const float* s, int nb, int k, int32_t* __restrict__ out,
+                           uint32_t* keys, uint32_t* hist, uint64_t* cand, uint64_t* sel,
+                           SelectShared& sh, int gtid, int bar_id) {
+  const int kk = k < nb ? k : nb;
+
+  if (kFromGlobal) {
+    for (int i = gtid; i < kSelHistBins; i += T) hist[i] = 0;
+    group_sync<T>(bar_id);
+    for (int base = 0; base < nb; base += 8 * T) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + j * T + gtid;
+        v[j] = i < nb ? __ldcg(s + i) : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + j * T + gtid;
+        if (i < nb) {
+          const uint32_t key = score_key(v[j]);
+          keys[i] = key;
+          atomicAdd(&hist[key >> kSelFirstShift], 1u);
+        }
+      }
+    }
+    group_sync<T>(bar_id);
+  }
+
+  enum Mode { kTakeAll, kTies, kCand };
+  Mode mode = kTakeAll;
+  uint32_t thr = 0;  // kTakeAll: key >= thr; kTies: key > thr, then ties by index
+  uint32_t need = static_cast<uint32_t>(kk);
+  uint32_t prefix = 0;  // kCand: candidates share the key bits [hi, 32) with prefix
+  int hi = 32;
+  if (kk > 0 && kk < nb) {
+    int nbits = kSelFirstBits;
+    bool first = true;
+    while (true) {
+      const int lo = hi - nbits;
+      const int nbins = 1 << nbits;
+      if (!first) {
+        const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
+        for (int i = gtid; i < nbins; i += T) hist[i] = 0;
+        group_sync<T>(bar_id);
+        for (int i = gtid; i < nb; i += T) {
+          const uint32_t key = keys[i];
+          if (((key ^ prefix) >> hi) == 0) atomicAdd(&hist[(key >> lo) & dmask], 1u);
+        }
+        group_sync<T>(bar_id);
+      }
+      first = false;
+      scan_bins<T>(hist, nbins, need, sh, gtid, bar_id);
+      const uint32_t digit = sh.digit, above = sh.above, cnt = sh.cnt;
+      need -= above;
+      prefix |= digit << lo;
+      hi = lo;
+      if (cnt == need) {
+        mode = kTakeAll;
+        thr = prefix;
+        break;
+      }
+      if (hi == 0) {
+        mode = kTies;
+        thr = prefix;
+        break;
+      }
+      if (cnt <= static_cast<uint32_t>(kSelCandMax)) {
+        mode = kCand;
+        break;
+      }
+      nbits = hi < 8 ? hi : 8;
+      group_sync<T>(bar_id);  // every thread has read sh before the next pass
+    }
+  }
+
+  if (kk > 0) {
+    // Gather: count, scan, write. Winners go to sel[0, n_win), candidates to
+    // cand[0, n_cand).
+    const uint32_t bin_top = (mode == kCand) ? (prefix | ((1u << hi) - 1u)) : 0u;
+    uint32_t n_w = 0, n_c = 0;
+    for (int i = gtid; i < nb; i += T) {
+      const uint32_t key = keys[i];
+      if (mode == kTakeAll) {
+        n_w += key >= thr ? 1u : 0u;
+      } else if (mode == kTies) {
+        n_w += key > thr ? 1u : 0u;
+      } else {
+        const bool w = key > bin_top;
+        n_w += w ? 1u : 0u;
+        n_c += (!w && ((key ^ prefix) >> hi) == 0) ? 1u : 0u;
+      }
+    }
+    uint32_t totals;
+    const uint32_t offs = group_excl_scan<T>((n_w << 16) | n_c, &totals, sh, gtid, bar_id);
+    uint32_t wo = offs >> 16, co = offs & 0xFFFFu;
+    const uint32_t n_win = totals >> 16, n_cand = totals & 0xFFFFu;
+    for (int i = gtid; i < nb; i += T) {
+      const uint32_t key = keys[i];
+      bool w, c = false;
+      if (mode == kTakeAll) {
+        w = key >= thr;
+      } else if (mode == kTies) {
+        w = key > thr;
+      } else {
+        w = key > bin_top;
+        c = !w && ((key ^ prefix) >> hi) == 0;
+      }
+      if (w) sel[wo++] = win_key(key, i);
+      if (c) cand[co++] = win_key(key, i);
+    }
+    group_sync<T>(bar_id);
+    if (mode == kCand) {
+      // The boundary bin's `need` largest candidates complete the winners.
+      const uint32_t nd = need;
+      split_rank<T>(cand, static_cast<int>(n_cand), gtid, [&](int e, uint32_t r) {
+        if (r < nd) sel[n_win + r] = cand[e];
+      });
+      group_sync<T>(bar_id);
+    } else if (mode == kTies) {
+      // Keys equal to thr, in index order, until `need` are taken.
+      uint32_t taken = 0;  // uniform over the group
+      for (int base = 0; base < nb && taken < need; base += T) {
+        const int i = base + gtid;
+        const bool tie = i < nb && keys[i] == thr;
+        uint32_t tot;
+        const uint32_t r = taken + group_excl_scan<T>(tie ? 1u : 0u, &tot, sh, gtid, bar_id);
+        if (tie && r < need) sel[n_win + r] = win_key(thr, i);
+        taken += tot;
+      }
+      group_sync<T>(bar_id);
+    }
+  }
+
+  // Output slot of every winner = its rank among the winners.
+  split_rank<T>(sel, kk, gtid, [&](int e, uint32_t r) {
+    out[r] = static_cast<int32_t>(~static_cast<uint32_t>(sel[e]));
+  });
+  for (int j = kk + gtid; j < k; j += T) out[j] = -1;
+}
+
+// ------------------------------------------------- register-resident keys
+// Thread gtid holds the keys of indices j*T + gtid, j < R (key 0 past nb: it
+// is below every finite score's key). Fewer instructions per element than
+// the shared-memory path, for rows with nb <= R*T.
+
+// Loads a row of scores (ld.global.cg) into registers and builds the
+// first-digit histogram (hist[kSelHistBins] in shared memory).
+template <int T, int R>
+__device__ __forceinline__ void load_keys_global(const float* s, int nb, uint32_t (&key)[R],
+                                                 uint32_t* hist, int gtid, int bar_id) {
+  for (int i = gtid; i < kSelHistBins; i += T) hist[i] = 0;
+  float v[R];
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    const int i = j * T + gtid;
+    v[j] = i < nb ? __ldcg(s + i) : 0.0f;
+  }
+  group_sync<T>(bar_id);
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    const int i = j * T + gtid;
+    key[j] = i < nb ? score_key(v[j]) : 0u;
+    if (i < nb) atomicAdd(&hist[key[j] >> kSelFirstShift], 1u);
+  }
+  group_sync<T>(bar_id);
+}
+
+// Loads keys already in shared memory (keys[nb]) into registers and builds
+// the first-digit histogram.
+template <int T, int R>
+__device__ __forceinline__ void load_keys_smem(const uint32_t* keys, int nb, uint32_t (&key)[R],
+                                               uint32_t* hist, int gtid, int bar_id) {
+  for (int i = gtid; i < kSelHistBins; i += T) hist[i] = 0;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    const int i = j * T + gtid;
+    key[j] = i < nb ? keys[i] : 0u;
+  }
+  group_sync<T>(bar_id);
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    if (j * T + gtid < nb) atomicAdd(&hist[key[j] >> kSelFirstShift], 1u);
+  }
+  group_sync<T>(bar_id);
+}
+
+// Top-k of one row whose keys are in registers and whose first-digit
+// histogram is complete in hist (see the loaders above).
+template <int T, int R>
+__device__ void select_row_regs(const uint32_t (&key)[R], int nb, int k, int32_t* __restrict__ out,
+                                uint32_t* hist, uint64_t* cand, uint64_t* sel, SelectShared& sh,
+                                int gtid, int bar_id) {
+  const int kk = k < nb ? k : nb;
+  enum Mode { kTakeAll, kTies, kCand };
+  Mode mode = kTakeAll;
+  uint32_t thr = 0;
+  uint32_t need = static_cast<uint32_t>(kk);
+  uint32_t prefix = 0;
+  int hi = 32;
+  if (kk > 0 && kk < nb) {
+    int nbits = kSelFirstBits;
+    bool first = true;
+    while (true) {
+      const int lo = hi - nbits;
+      const int nbins = 1 << nbits;
+      if (!first) {
+        const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
+        for (int i = gtid; i < nbins; i += T) hist[i] = 0;
+        group_sync<T>(bar_id);
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          if (j * T + gtid < nb && ((key[j] ^ prefix) >> hi) == 0)
+            atomicAdd(&hist[(key[j] >> lo) & dmask], 1u);
+        }
+        group_sync<T>(bar_id);
+      }
+      first = false;
+      scan_bins<T>(hist, nbins, need, sh, gtid, bar_id);
+      const uint32_t digit = sh.digit, above = sh.above, cnt = sh.cnt;
+      need -= above;
+      prefix |= digit << lo;
+      hi = lo;
+      if (cnt == need) {
+        mode = kTakeAll;
+        thr = prefix;
+        break;
+      }
+      if (hi == 0) {
+        mode = kTies;
+        thr = prefix;
+        break;
+      }
+      if (cnt <= static_cast<uint32_t>(kSelCandMax)) {
+        mode = kCand;
+        break;
+      }
+      nbits = hi < 8 ? hi : 8;
+      group_sync<T>(bar_id);
+    }
+  }
+
+  if (kk > 0) {
+    // Winner / candidate flags per register key (key 0 never qualifies).
+    uint32_t wmask = 0, cmask = 0;
+    if (mode == kCand) {
+      const uint32_t bin_top = prefix | ((1u << hi) - 1u);
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const bool valid = j * T + gtid < nb;
+        const bool w = valid && key[j] > bin_top;
+        const bool c = valid && !w && ((key[j] ^ prefix) >> hi) == 0;
+        wmask |= (w ? 1u : 0u) << j;
+        cmask |= (c ? 1u : 0u) << j;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const bool valid = j * T + gtid < nb;
+        const bool w = valid && (mode == kTakeAll ? key[j] >= thr : key[j] > thr);
+        wmask |= (w ? 1u : 0u) << j;
+      }
+    }
+    uint32_t totals;
+    const uint32_t offs = group_excl_scan<T>((static_cast<uint32_t>(__popc(wmask)) << 16) |
+                                                 static_cast<uint32_t>(__popc(cmask)),
+                                             &totals, sh, gtid, bar_id);
+    uint32_t wo = offs >> 16, co = offs & 0xFFFFu;
+    const uint32_t n_win = totals >> 16, n_cand = totals & 0xFFFFu;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      if (wmask & (1u << j)) sel[wo++] = win_key(key[j], j * T + gtid);
+      if (cmask & (1u << j)) cand[co++] = win_key(key[j], j * T + gtid);
+    }
+    group_sync<T>(bar_id);
+    if (mode == kCand) {
+      const uint32_t nd = need;
+      split_rank<T>(cand, static_cast<int>(n_cand), gtid, [&](int e, uint32_t r) {
+        if (r < nd) sel[n_win + r] = cand[e];
+      });
+      group_sync<T>(bar_id);
+    } else if (mode == kTies) {
+      uint32_t taken = 0;  // uniform over the group; slices j in index order
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        if (taken >= need) break;
+        const int i = j * T + gtid;
+        const bool tie = i < nb && key[j] == thr;
+        uint32_t tot;
+        const uint32_t r = taken + group_excl_scan<T>(tie ? 1u : 0u, &tot, sh, gtid, bar_id);
+        if (tie && r < need) sel[n_win + r] = win_key(thr, i);
+        taken += tot;
+      }
+      group_sync<T>(bar_id);
+    }
+  }
+
+  // Output slot of every winner: its rank among the winners.
+  split_rank<T>(sel, kk, gtid, [&](int e, uint32_t r) {
+    out[r] = static_cast<int32_t>(~static_cast<uint32_t>(sel[e]));
+  });
+  for (int j = kk + gtid; j < k; j += T) out[j] = -1;
+}
+
+}  // namespace qsa
