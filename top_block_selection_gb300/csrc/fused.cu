@@ -367,10 +367,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
   // ---------------------------------------------------------- select
   // One row at a time with the kWork threads. hist / cand / sel (and, for
   // long rows, keys) reuse the dead operand tiles.
-  uint64_t* cand = reinterpret_cast<uint64_t*>(smem);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(hist + kSelHistBins);
   uint64_t* sel = cand + kSelCandMax;
-  uint32_t* hist = reinterpret_cast<uint32_t*>(sel + a.k);
-  uint32_t* keys = hist + kSelHistBins;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(sel + a.k);
   for (int r = 0; r < rows_here; ++r) {
     const int qi = q0 + rank + r * kCluster;
     if (qi >= a.nq) break;

@@ -19,10 +19,10 @@ __global__ void __launch_bounds__(kSelThreads)
                   int32_t* __restrict__ ids) {
   extern __shared__ __align__(16) uint8_t sm_raw[];
   __shared__ SelectShared sh;
-  uint64_t* cand = reinterpret_cast<uint64_t*>(sm_raw);                 // [kSelCandMax]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sm_raw);                 // [kSelHistBins]
+  uint64_t* cand = reinterpret_cast<uint64_t*>(hist + kSelHistBins);     // [kSelCandMax]
   uint64_t* sel = cand + kSelCandMax;                                    // [k]
-  uint32_t* hist = reinterpret_cast<uint32_t*>(sel + k);                 // [kSelHistBins]
-  uint32_t* keys = hist + kSelHistBins;                                  // [nb] (long rows)
+  uint32_t* keys = reinterpret_cast<uint32_t*>(sel + k);                 // [nb] (long rows)
   const int64_t row = blockIdx.x;
   const float* s = scores + row * nb;
   int32_t* out = ids + row * k;

@@ -108,35 +108,62 @@ __device__ __forceinline__ void split_rank(const uint64_t* x, int n, int gtid, E
   }
 }
 
-// Finds the digit of the bins [0, nbins) holding the need-th largest key
+// Finds the digit of the bins [0, NBINS) holding the need-th largest key
 // (counting from the top bin down); writes digit, count above it and its own
-// count to sh. Thread t owns bins [nbins - (t+1)B, nbins - tB).
-template <int T>
-__device__ __forceinline__ void scan_bins(const uint32_t* hist, int nbins, uint32_t need,
-                                          SelectShared& sh, int gtid, int bar_id) {
-  const int B = nbins >= T ? nbins / T : 1;
-  const int top = nbins - gtid * B;
-  uint32_t local = 0;
-  if (top > 0) {
-    for (int j = 1; j <= B; ++j) local += hist[top - j];
+// count to sh. Thread t owns the B = NBINS / T bins [NBINS - (t+1)B, NBINS -
+// tB), read with 16-byte loads when B is a multiple of 4.
+template <int T, int NBINS>
+__device__ __forceinline__ void scan_bins_fixed(const uint32_t* hist, uint32_t need,
+                                                SelectShared& sh, int gtid, int bar_id) {
+  constexpr int B = NBINS >= T ? NBINS / T : 1;
+  const int base = NBINS - (gtid + 1) * B;  // lowest bin of this thread (may be < 0)
+  uint32_t c[B];
+  if (base >= 0) {
+    if constexpr (B % 4 == 0) {
+#pragma unroll
+      for (int j = 0; j < B; j += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(hist + base + j);
+        c[j] = v.x;
+        c[j + 1] = v.y;
+        c[j + 2] = v.z;
+        c[j + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < B; ++j) c[j] = hist[base + j];
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < B; ++j) c[j] = 0;
   }
+  uint32_t local = 0;
+#pragma unroll
+  for (int j = 0; j < B; ++j) local += c[j];
   uint32_t tot;
   const uint32_t excl = group_excl_scan<T>(local, &tot, sh, gtid, bar_id);
-  const uint32_t incl = excl + local;
-  if (excl < need && need <= incl) {
+  if (excl < need && need <= excl + local) {
     uint32_t run = excl;
-    for (int j = 1; j <= B; ++j) {
-      const uint32_t c = hist[top - j];
-      if (run + c >= need) {
-        sh.digit = static_cast<uint32_t>(top - j);
+    bool found = false;
+#pragma unroll
+    for (int j = B - 1; j >= 0; --j) {
+      if (!found && run + c[j] >= need) {
+        sh.digit = static_cast<uint32_t>(base + j);
         sh.above = run;
-        sh.cnt = c;
-        break;
+        sh.cnt = c[j];
+        found = true;
       }
-      run += c;
+      run += c[j];
     }
   }
   group_sync<T>(bar_id);
+}
+
+// The same for a run-time number of bins (2048 or 256).
+template <int T>
+__device__ __forceinline__ void scan_bins(const uint32_t* hist, int nbins, uint32_t need,
+                                          SelectShared& sh, int gtid, int bar_id) {
+  if (nbins == kSelHistBins) scan_bins_fixed<T, kSelHistBins>(hist, need, sh, gtid, bar_id);
+  else scan_bins_fixed<T, 256>(hist, need, sh, gtid, bar_id);
 }
 
 // Top-k of one row, keys staged in shared memory (any nb up to the shared
@@ -144,8 +171,8 @@ __device__ __forceinline__ void scan_bins(const uint32_t* hist, int nbins, uint3
 // it may have been written by other CTAs of the same kernel) into keys[] and
 // the first-digit histogram is built here; otherwise keys[0..nb) and the
 // first-digit histogram in hist[] must already be complete.
-// Shared arrays of this group: keys[nb], hist[kSelHistBins], cand[kSelCandMax],
-// sel[min(k, nb)].
+// Shared arrays of this group: keys[nb], hist[kSelHistBins] (16-byte
+// aligned), cand[kSelCandMax], sel[min(k, nb)].
 template <int T, bool kFromGlobal>
 __device__ void select_row_smem(const float* s, int nb, int k, int32_t* __restrict__ out,
                            uint32_t* keys, uint32_t* hist, uint64_t* cand, uint64_t* sel,
@@ -189,7 +216,7 @@ __device__ void select_row_smem(const float* s, int nb, int k, int32_t* __restri
       const int nbins = 1 << nbits;
       if (!first) {
         const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
-        for (int i = gtid; i < nbins; i += T) hist[i] = 0;
+        for (int i = gtid; i < 256; i += T) hist[i] = 0;  // refinement scans read 256 bins
         group_sync<T>(bar_id);
         for (int i = gtid; i < nb; i += T) {
           const uint32_t key = keys[i];
@@ -354,7 +381,7 @@ __device__ void select_row_regs(const uint32_t (&key)[R], int nb, int k, int32_t
       const int nbins = 1 << nbits;
       if (!first) {
         const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
-        for (int i = gtid; i < nbins; i += T) hist[i] = 0;
+        for (int i = gtid; i < 256; i += T) hist[i] = 0;  // refinement scans read 256 bins
         group_sync<T>(bar_id);
 #pragma unroll
         for (int j = 0; j < R; ++j) {
