@@ -41,9 +41,15 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic per launch from an ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed by kernel, with the SHA-256 of the kernel's
-# source file at capture time; a stale entry reports null.
-NCU_TRAFFIC = {}
+# dram__bytes_write.sum), keyed by kernel, with the SHA-256 (first 16 hex
+# digits) of the kernel's source files at capture time; an entry whose
+# sources have changed since reports null. The capture and its command are
+# summarised in profiles/fused_step_kernel_long128k.md.
+NCU_TRAFFIC = {
+    "fused_step_kernel": {"bytes_per_launch": 1640960, "sources": ["fused.cu", "select_row.cuh"],
+                          "source_sha": "724c481832df3328",
+                          "workload": "long128k_nq256_h8_d128_kv131072"},
+}
 
 
 def parse_args():
@@ -201,15 +207,17 @@ def time_region(torch, stream, replay, reps_min, seconds, barrier=None):
     return out
 
 
-def kernel_source_sha(name):
-    path = os.path.join(ROOT, "top_block_selection_gb300", "csrc", name)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def kernel_source_sha(names):
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "top_block_selection_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
-def traffic_for(kernel, source, w):
+def traffic_for(kernel, w):
     e = NCU_TRAFFIC.get(kernel)
-    if not e or e.get("source_sha") != kernel_source_sha(source) or e.get("workload") != w.name:
+    if not e or e.get("workload") != w.name or e.get("source_sha") != kernel_source_sha(e["sources"]):
         return None
     return e["bytes_per_launch"]
 
@@ -322,7 +330,7 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": step_bytes / t_step / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = traffic_for("fused_step_kernel", "fused.cu", w)
+    roof["traffic"] = traffic_for("fused_step_kernel", w)
     roof["kernel"] = "fused_step_kernel (qsa_select_step: one launch per step)"
     roof["peak_source"] = f"{peak_src} (fp16 dense taken equal to the measured bf16 burst)"
     roof["algorithmic"] = {"flops": step_flops, "bytes": step_bytes,

@@ -182,6 +182,17 @@ qsa_status qsa_select_step_host(const float* q32_host, const uint16_t* kb_host, 
  */
 qsa_status qsa_device_status(int clear, uint32_t* bits, qsa_stream_t stream);
 
+/*
+ * qsa_selftest_bounded_wait - failure-detection self-test. Launches one
+ * kernel that waits on a barrier nothing completes, for at most timeout_ns
+ * (1 ns .. 1 s), then gives up and sets bit 31 of the device status word,
+ * exactly as a real kernel does when one of its bounded waits runs out. The
+ * GPU context stays usable. A following qsa_device_status() returns
+ * QSA_ERR_TIMEOUT with that bit set (and clears it when asked).
+ * Errors: QSA_ERR_INVALID_ARG for a timeout outside the range.
+ */
+qsa_status qsa_selftest_bounded_wait(uint64_t timeout_ns, qsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -115,6 +115,11 @@ def test_convert_and_step_reject_bad_arguments_on_host(lib):
     assert step(A + 2, A) == MISALIGNED
 
 
+def test_selftest_rejects_bad_timeout_on_host(lib):
+    assert lib.qsa_selftest_bounded_wait(0, None) == INVALID
+    assert lib.qsa_selftest_bounded_wait(2_000_000_000, None) == INVALID
+
+
 def test_binding_refuses_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(tbs, "_LIB", None)
     monkeypatch.setenv("QSA_LIBRARY", str(tmp_path / "missing.so"))

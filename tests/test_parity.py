@@ -266,6 +266,24 @@ def test_negative_control_on_gpu_scores(tbs):
     assert not orc.bound_report(bad, s_ref, B)["ok"]
 
 
+def test_bounded_wait_timeout_is_reported(tbs):
+    """A wait that nothing completes gives up after its bound, sets the
+    status word, and leaves the context usable."""
+    st, bits = tbs.qsa_device_status(clear=True)
+    assert st == 0 and bits == 0
+    tbs.qsa_selftest_bounded_wait(2_000_000)          # 2 ms
+    st, bits = tbs.qsa_device_status(clear=False)
+    assert st == 6 and bits == (1 << 31)               # QSA_ERR_TIMEOUT, self-test bit
+    st, bits = tbs.qsa_device_status(clear=True)      # read and clear
+    assert st == 6
+    st, bits = tbs.qsa_device_status(clear=True)
+    assert st == 0 and bits == 0
+    # the context still works
+    w = qi.WORKLOADS[0]
+    q, kb = qi.make_inputs(w)
+    check_case(tbs, q, kb, w.n_kv, w.block, w.k, "after-timeout")
+
+
 def test_device_status_clear(tbs):
     st, bits = tbs.qsa_device_status(clear=True)
     assert st == 0 and bits == 0

@@ -16,7 +16,8 @@ __all__ = [
     "QsaError", "load_library", "library_path", "qsa_abi_version", "qsa_status_str",
     "qsa_last_cuda_error", "qsa_arm",
     "qsa_num_blocks", "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select",
-    "qsa_select_step", "qsa_select_step_host", "qsa_device_status", "EXPORTED_SYMBOLS",
+    "qsa_select_step", "qsa_select_step_host", "qsa_device_status", "qsa_selftest_bounded_wait",
+    "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -26,7 +27,7 @@ _LIB = None
 EXPORTED_SYMBOLS = (
     "qsa_abi_version", "qsa_status_str", "qsa_last_cuda_error", "qsa_arm", "qsa_num_blocks",
     "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select", "qsa_select_step",
-    "qsa_select_step_host", "qsa_device_status",
+    "qsa_select_step_host", "qsa_device_status", "qsa_selftest_bounded_wait",
 )
 
 STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED_GEOMETRY",
@@ -72,6 +73,7 @@ def load_library():
         "qsa_select_step_host": (ctypes.c_int, [vp, vp, i32, i32, i32, i64, i32, i32, vp, vp,
                                                 vp, vp, vp, vp, vp, vp]),
         "qsa_device_status": (ctypes.c_int, [ctypes.c_int, u32p, vp]),
+        "qsa_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint64, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -284,3 +286,15 @@ def qsa_device_status(clear: bool = True, device=None):
         st = lib.qsa_device_status(1 if clear else 0, ctypes.byref(bits),
                                    ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
     return st, bits.value
+
+
+def qsa_selftest_bounded_wait(timeout_ns: int = 1_000_000, device=None):
+    """Run the bounded-wait self-test kernel on the current stream (it gives
+    up after timeout_ns and records a timeout in the status word)."""
+    torch = _torch()
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(lib.qsa_selftest_bounded_wait(timeout_ns,
+                                             ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)),
+               "qsa_selftest_bounded_wait")

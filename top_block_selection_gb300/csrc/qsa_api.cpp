@@ -210,6 +210,14 @@ qsa_status qsa_select_step_host(const float* q32_host, const uint16_t* kb_host, 
   return QSA_OK;
 }
 
+qsa_status qsa_selftest_bounded_wait(uint64_t timeout_ns, qsa_stream_t stream) {
+  if (timeout_ns == 0 || timeout_ns > 1000000000ull) return QSA_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  qsa_status st = device_or_error(&dev);
+  if (st != QSA_OK) return st;
+  return from_cuda(qsa::launch_selftest_wait(*dev, timeout_ns, as_cuda(stream)));
+}
+
 qsa_status qsa_device_status(int clear, uint32_t* bits, qsa_stream_t stream) {
   const DeviceInfo* dev = nullptr;
   qsa_status st = device_or_error(&dev);

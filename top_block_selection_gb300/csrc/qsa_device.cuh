@@ -13,6 +13,7 @@ enum : uint32_t {
   kErrScoreLoadTimeout = 1u << 0,  // TMA tile never arrived
   kErrScoreMmaTimeout = 1u << 1,   // tcgen05.commit never arrived
   kErrFusedWaitTimeout = 1u << 2,  // a cross-CTA dependency never completed
+  kErrSelftestTimeout = 1u << 31,  // the bounded-wait self-test ran out (expected)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

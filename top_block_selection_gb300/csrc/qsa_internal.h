@@ -70,6 +70,9 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
 cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k, int32_t* ids,
                           const DeviceInfo& dev, cudaStream_t stream);
 
+// Launches the bounded-wait self-test (see qsa_selftest_bounded_wait).
+cudaError_t launch_selftest_wait(const DeviceInfo& dev, uint64_t timeout_ns, cudaStream_t stream);
+
 constexpr int kMaxSelectK = 1024;
 constexpr int kMaxSelectNb = 32768;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s bound on any device-side wait

@@ -2,6 +2,7 @@
 // attributes, one-time kernel setup, and the driver's tensor-map encoder.
 #include <mutex>
 
+#include "qsa_device.cuh"
 #include "qsa_internal.h"
 
 namespace qsa {
@@ -52,6 +53,23 @@ const DeviceInfo* current_device(cudaError_t* err) {
   d.ready = true;
   *err = cudaSuccess;
   return &d;
+}
+
+// Waits on an mbarrier that nothing arrives on, for at most timeout_ns, then
+// records the expiry in the status word: the bounded-wait path of every
+// kernel, exercised on purpose without hanging or faulting the GPU.
+__global__ void selftest_wait_kernel(uint32_t* status, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+    if (!mbar_wait_bounded(&bar, 0, timeout_ns)) atomicOr(status, kErrSelftestTimeout);
+  }
+}
+
+cudaError_t launch_selftest_wait(const DeviceInfo& dev, uint64_t timeout_ns, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(dev.status_word, timeout_ns);
+  return cudaGetLastError();
 }
 
 EncodeTiledFn encode_tiled_fn() {
