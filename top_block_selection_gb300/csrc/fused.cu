@@ -140,6 +140,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
   __shared__ int failed;
   __shared__ float tail_acc[256];
   __shared__ SelectShared sel_sh;
+  __shared__ GroupShared sel_gsh;
 
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -160,6 +161,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
   const uint32_t rows_base = smem_u32(smem + a.rows_off);
   const bool producer_warp = warp == kProducerWarp;
 
+  // Programmatic dependent launch: the next kernel on the stream may start its
+  // own set-up now; this kernel reads nothing produced by earlier work on the
+  // stream before griddepcontrol.wait below.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == kProducerWarp * 32) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_full[s], 1);
@@ -171,8 +176,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
     failed = 0;
     fence_mbarrier_init();
     if (n_local > 0) tma_prefetch_desc(&tm_kb);
+    if (!kF32Q && need_q) tma_prefetch_desc(&tm_q);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == kProducerWarp * 32) {
     if (!kF32Q && need_q) {
-      tma_prefetch_desc(&tm_q);
       mbar_arrive_expect_tx(&bar_q, static_cast<uint32_t>(a.n_chunks * a.bn * kFRowBytes));
       for (int c = 0; c < a.n_chunks; ++c)
         tma_load_2d(sQ + c * a.bn * kFRowBytes, &tm_q, c * kFKAtom, col0, &bar_q);
@@ -233,7 +241,6 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = tmem_slot;
-  if (a.dsmem) cluster_wait_acquire();
 
   if (producer_warp) {
     // ---------------------------------------------------- producer / MMA
@@ -280,7 +287,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
       }
     }
     __syncwarp();
+    if (a.dsmem) cluster_wait_acquire();  // pairs with the early arrive
   } else {
+    // Peers' shared memory is written below (keys over DSMEM): every CTA of
+    // the cluster must have started, which the early arrive and one wait per
+    // thread guarantee. Each warp waits just before its first remote store
+    // (warp-uniform flag), which keeps the cluster's start skew off the
+    // loads, the MMAs and the tail's dot products.
+    bool waited = !a.dsmem;
     // ------------------------------ tail block (warps 0..3 of the owner)
     if (tail_owner && warp < 4) {
       if (!kF32Q && !mbar_wait_bounded(&bar_q, 0, a.timeout_ns)) {
@@ -303,6 +317,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
         tail_acc[p] = acc;
       }
       asm volatile("bar.sync 3, 128;" ::: "memory");
+      if (!waited) {
+        cluster_wait_acquire();
+        waited = true;
+      }
       for (int ql = tid; ql * H < pairs; ql += 128) {
         float s = 0.0f;
 #pragma unroll
@@ -327,6 +345,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
         break;
       }
       tc_fence_after_sync();
+      if (!waited) {
+        cluster_wait_acquire();
+        waited = true;
+      }
       if (failed) break;
       const int b = (rank + t * kCluster) * kFTileM + quarter * 32 + lane;
       const bool b_ok = b < a.n_full;
@@ -353,6 +375,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
       tc_fence_before_sync();
       mbar_arrive(&bar_acc_empty[s]);
     }
+    if (!waited) cluster_wait_acquire();
   }
 
   tc_fence_before_sync();
@@ -365,12 +388,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
   if (producer_warp) return;  // the select runs on the kWork threads
 
   // ---------------------------------------------------------- select
-  // One row at a time with the kWork threads. hist / cand / sel (and, for
-  // long rows, keys) reuse the dead operand tiles.
+  // One row at a time with the kWork threads (the lowest latency per row).
+  // Keys come from the row regions (DSMEM mode) or from global memory;
+  // hist / cand / sel reuse the dead operand tiles.
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem);
   uint64_t* cand = reinterpret_cast<uint64_t*>(hist + kSelHistBins);
-  uint64_t* sel = cand + kSelCandMax;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(sel + a.k);
+  uint64_t* sel = cand + kSelBinMax;
+  uint32_t* staged = reinterpret_cast<uint32_t*>(sel + a.k);
   for (int r = 0; r < rows_here; ++r) {
     const int qi = q0 + rank + r * kCluster;
     if (qi >= a.nq) break;
@@ -388,7 +412,25 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
       else load_keys_global<kWork, 16>(row, a.nb, key, hist, tid, 1);
       select_row_regs<kWork, 16>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1);
     } else {
-      select_row_smem<kWork, true>(row, a.nb, a.k, out, keys, hist, cand, sel, sel_sh, tid, 1);
+      const uint32_t* keys = rk;
+      if (!a.dsmem) {
+        for (int b0 = 0; b0 < a.nb; b0 += 8 * kWork) {
+          float v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int i = b0 + j * kWork + tid;
+            v[j] = i < a.nb ? __ldcg(row + i) : 0.0f;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int i = b0 + j * kWork + tid;
+            if (i < a.nb) staged[i] = score_key(v[j]);
+          }
+        }
+        group_sync<kWork>(1);
+        keys = staged;
+      }
+      select_row_g<kWork / 32>(keys, a.nb, a.k, out, hist, cand, sel, sel_gsh, tid, 1);
     }
     group_sync<kWork>(1);
   }
@@ -482,16 +524,16 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
   const int rows_per_cta = (qg + kCluster - 1) / kCluster;
   const size_t operand_bytes = static_cast<size_t>(a.n_chunks) * (bn + 2 * kFTileM) * kFRowBytes;
   const size_t budget = static_cast<size_t>(dev.max_smem_optin) - g_fused_static_smem - 1024;
-  // Select scratch in the operand region after the epilogue: cand, sel,
-  // hist, and the keys of a long row (> 4096 blocks) read from global.
-  size_t sel_bytes = (static_cast<size_t>(kSelCandMax) + p.k) * sizeof(uint64_t) +
-                     kSelHistBins * sizeof(uint32_t);
-  if (p.nb > 16 * kWork) sel_bytes += static_cast<size_t>(p.nb) * sizeof(uint32_t);
+  // Select scratch in the operand region after the epilogue: hist, cand, sel,
+  // and (global mode, long rows) the row's staged keys.
+  const size_t core = kSelHistBins * sizeof(uint32_t) +
+                      (static_cast<size_t>(kSelBinMax) + p.k) * sizeof(uint64_t);
   // DSMEM mode when the keys of the rows this CTA selects fit beside the
-  // operand tiles (register path only: nb <= 4096).
-  const size_t row_bytes = static_cast<size_t>((a.nb + 3) & ~3) * sizeof(uint32_t);
-  const size_t rows_off = (std::max(operand_bytes, sel_bytes) + 1023) & ~static_cast<size_t>(1023);
-  a.dsmem = (p.nb <= 16 * kWork && rows_off + rows_per_cta * row_bytes <= budget) ? 1 : 0;
+  // operand tiles.
+  const size_t row_bytes = (static_cast<size_t>(a.nb) * sizeof(uint32_t) + 15) & ~static_cast<size_t>(15);
+  const size_t rows_off = (std::max(operand_bytes, core) + 1023) & ~static_cast<size_t>(1023);
+  a.dsmem = (rows_off + rows_per_cta * row_bytes <= budget) ? 1 : 0;
+  const size_t sel_bytes = a.dsmem ? core : core + static_cast<size_t>(a.nb) * sizeof(uint32_t);
   a.sel_bytes = static_cast<uint32_t>(sel_bytes);
   a.row_bytes = static_cast<uint32_t>(row_bytes);
   a.rows_off = static_cast<uint32_t>(rows_off);
@@ -507,25 +549,22 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
   if (p.q32 == nullptr &&
       !encode_f16_2d(&tm_q, p.q16, p.D, static_cast<uint64_t>(p.nq) * p.H, kFKAtom, bn))
     return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>(groups * kCluster));
   const bool f32q = p.q32 != nullptr;
-#define QSA_FUSED_LAUNCH(HH)                                                               \
-  case HH:                                                                                 \
-    if (f32q)                                                                              \
-      fused_step_kernel<HH, true><<<grid, kFThreads, smem, stream>>>(tm_kb, tm_q, a);      \
-    else                                                                                   \
-      fused_step_kernel<HH, false><<<grid, kFThreads, smem, stream>>>(tm_kb, tm_q, a);     \
-    break;
-  switch (p.H) {
-    QSA_FUSED_LAUNCH(1)
-    QSA_FUSED_LAUNCH(2)
-    QSA_FUSED_LAUNCH(4)
-    QSA_FUSED_LAUNCH(8)
-    QSA_FUSED_LAUNCH(16)
-    QSA_FUSED_LAUNCH(32)
-    default: return cudaErrorInvalidValue;
-  }
-#undef QSA_FUSED_LAUNCH
+  const void* fn = fused_kernel_for(p.H, f32q);
+  if (fn == nullptr) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(groups * kCluster));
+  cfg.blockDim = dim3(kFThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&tm_kb, &tm_q, &a};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

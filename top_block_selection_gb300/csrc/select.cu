@@ -2,69 +2,81 @@
 // part 1 and pull request 856, "Arithmetic contract and parity": the top-k
 // over the block scores, here with a block-index tie-break).
 //
-// One CTA of kSelThreads threads per query row (see select_row.cuh for the
-// algorithm): the row's keys stay in registers (8 or 16 per thread) for rows
-// up to 4096 blocks, in shared memory beyond; the first 11-bit radix digit's
-// histogram is built while the row is read; a suffix scan finds the boundary
-// bin; a small boundary bin is ranked exactly; the winners are rank-sorted.
+// A CTA of kSelThreads threads selects kSelRowsPerCta rows, kSelG warps per
+// row (see select_row_g in select_row.cuh for the algorithm): the row's keys
+// are staged in shared memory, the first 11-bit radix digit finds the
+// boundary bin, the boundary bin's keys are compacted and refined, and the
+// winners are rank-sorted.
 #include "qsa_internal.h"
 #include "select_row.cuh"
 
 namespace qsa {
 
 constexpr int kSelThreads = 256;
+constexpr int kSelG = 4;                          // warps per row
+constexpr int kSelMaxGroups = kSelThreads / (32 * kSelG);  // rows per CTA at most
+
+// Shared bytes of one row's group: hist, cand, sel (k), keys (nb).
+__host__ __device__ inline size_t select_group_bytes(int32_t nb, int32_t k) {
+  size_t b = kSelHistBins * sizeof(uint32_t) + (static_cast<size_t>(kSelBinMax) + k) * sizeof(uint64_t) +
+             static_cast<size_t>(nb) * sizeof(uint32_t);
+  return (b + 15) & ~static_cast<size_t>(15);
+}
 
 __global__ void __launch_bounds__(kSelThreads)
-    select_kernel(const float* __restrict__ scores, int32_t nb, int32_t k,
+    select_kernel(const float* __restrict__ scores, int32_t nq, int32_t nb, int32_t k,
                   int32_t* __restrict__ ids) {
   extern __shared__ __align__(16) uint8_t sm_raw[];
-  __shared__ SelectShared sh;
-  uint32_t* hist = reinterpret_cast<uint32_t*>(sm_raw);                 // [kSelHistBins]
-  uint64_t* cand = reinterpret_cast<uint64_t*>(hist + kSelHistBins);     // [kSelCandMax]
-  uint64_t* sel = cand + kSelCandMax;                                    // [k]
-  uint32_t* keys = reinterpret_cast<uint32_t*>(sel + k);                 // [nb] (long rows)
-  const int64_t row = blockIdx.x;
+  __shared__ GroupShared sh[kSelMaxGroups];
+  constexpr int T = 32 * kSelG;
+  const int groups = blockDim.x / T;  // rows per CTA, chosen at launch to fit shared memory
+  const int g = threadIdx.x / T;
+  const int gtid = threadIdx.x % T;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * groups + g;
+  if (row >= nq) return;  // whole groups leave together; no CTA-wide barrier follows
+  uint8_t* base = sm_raw + g * select_group_bytes(nb, k);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(base);                 // [kSelHistBins]
+  uint64_t* cand = reinterpret_cast<uint64_t*>(hist + kSelHistBins);  // [kSelBinMax]
+  uint64_t* sel = cand + kSelBinMax;                                  // [k]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(sel + k);              // [nb]
   const float* s = scores + row * nb;
-  int32_t* out = ids + row * k;
-  if (nb <= 8 * kSelThreads) {
-    uint32_t key[8];
-    load_keys_global<kSelThreads, 8>(s, nb, key, hist, threadIdx.x, 1);
-    select_row_regs<kSelThreads, 8>(key, nb, k, out, hist, cand, sel, sh, threadIdx.x, 1);
-  } else if (nb <= 16 * kSelThreads) {
-    uint32_t key[16];
-    load_keys_global<kSelThreads, 16>(s, nb, key, hist, threadIdx.x, 1);
-    select_row_regs<kSelThreads, 16>(key, nb, k, out, hist, cand, sel, sh, threadIdx.x, 1);
-  } else {
-    select_row_smem<kSelThreads, true>(s, nb, k, out, keys, hist, cand, sel, sh, threadIdx.x, 1);
+  for (int b0 = 0; b0 < nb; b0 += 8 * T) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = b0 + j * T + gtid;
+      v[j] = i < nb ? __ldcg(s + i) : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = b0 + j * T + gtid;
+      if (i < nb) keys[i] = score_key(v[j]);
+    }
   }
+  group_sync<T>(1 + g);
+  select_row_g<kSelG>(keys, nb, k, ids + row * k, hist, cand, sel, sh[g], gtid, 1 + g);
 }
-
-namespace {
-size_t select_smem_bytes(int32_t nb, int32_t k) {
-  size_t b = (static_cast<size_t>(kSelCandMax) + k) * sizeof(uint64_t) + kSelHistBins * sizeof(uint32_t);
-  if (nb > 16 * kSelThreads) b += static_cast<size_t>(nb) * sizeof(uint32_t);
-  return b;
-}
-}  // namespace
 
 cudaError_t init_select_kernels(const DeviceInfo& dev) {
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&select_kernel));
   if (e != cudaSuccess) return e;
-  const size_t most = select_smem_bytes(kMaxSelectNb, kMaxSelectK);
-  const size_t room = static_cast<size_t>(dev.max_smem_optin) - fa.sharedSizeBytes;
   return cudaFuncSetAttribute(reinterpret_cast<const void*>(&select_kernel),
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(most < room ? most : room));
+                              dev.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
 }
 
 cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k, int32_t* ids,
                           const DeviceInfo& dev, cudaStream_t stream) {
   if (nq <= 0) return cudaSuccess;
-  const size_t smem = select_smem_bytes(nb, k);
-  if (smem + sizeof(SelectShared) > static_cast<size_t>(dev.max_smem_optin))
-    return cudaErrorInvalidValue;
-  select_kernel<<<static_cast<unsigned>(nq), kSelThreads, smem, stream>>>(scores, nb, k, ids);
+  const size_t per = select_group_bytes(nb, k);
+  const size_t room = static_cast<size_t>(dev.max_smem_optin) - sizeof(GroupShared) * kSelMaxGroups;
+  int groups = kSelMaxGroups;
+  while (groups > 1 && static_cast<size_t>(groups) * per > room) groups >>= 1;
+  if (per > room) return cudaErrorInvalidValue;
+  const int64_t grid = (static_cast<int64_t>(nq) + groups - 1) / groups;
+  select_kernel<<<static_cast<unsigned>(grid), groups * 32 * kSelG, groups * per, stream>>>(
+      scores, nq, nb, k, ids);
   return cudaGetLastError();
 }
 

@@ -100,7 +100,7 @@ __device__ __forceinline__ void split_rank(const uint64_t* x, int n, int gtid, E
     uint32_t r = 0;
     if (valid) {
       int m = sub;
-#pragma unroll 4
+#pragma unroll 8
       for (; m < n; m += P) r += x[m] > me ? 1u : 0u;
     }
     for (int o = 1; o < P; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
@@ -471,6 +471,311 @@ __device__ void select_row_regs(const uint32_t (&key)[R], int nb, int k, int32_t
   }
 
   // Output slot of every winner: its rank among the winners.
+  split_rank<T>(sel, kk, gtid, [&](int e, uint32_t r) {
+    out[r] = static_cast<int32_t>(~static_cast<uint32_t>(sel[e]));
+  });
+  for (int j = kk + gtid; j < k; j += T) out[j] = -1;
+}
+
+// ------------------------------------------------ G-warp select, keys in smem
+// A group of G warps (T = 32 G threads) selects one row whose keys are in
+// shared memory. Per-element work is a histogram increment and two compares;
+// everything else is a fixed cost per warp, which is why a row gets only a
+// few warps. After the first 11-bit digit, the boundary bin's keys (at most
+// kSelBinMax of them) are compacted and only they are refined, 8 bits at a
+// time, until the keys still needed fill a bin or at most kSelRankMax remain,
+// which are ranked pairwise.
+constexpr int kSelBinMax = 256;
+constexpr int kSelRankMax = 32;
+
+struct GroupShared {
+  uint32_t wsum[8];
+  uint32_t digit, above, cnt, seg;
+};
+
+// Exclusive scan over the group; ends with a barrier (wsum reusable after).
+template <int T>
+__device__ __forceinline__ uint32_t gscan(uint32_t v, uint32_t* total, GroupShared& sh, int gtid,
+                                          int bar_id) {
+  constexpr int W = T / 32;
+  const int lane = gtid & 31, gw = gtid >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  if (W == 1) {
+    *total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    __syncwarp();
+    return incl - v;
+  }
+  if (lane == 31) sh.wsum[gw] = incl;
+  group_sync<T>(bar_id);
+  uint32_t before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < W; ++w) {
+    const uint32_t x = sh.wsum[w];
+    before += (w < gw) ? x : 0u;
+    tot += x;
+  }
+  group_sync<T>(bar_id);
+  *total = tot;
+  return before + incl - v;
+}
+
+// Boundary digit among NB bins: the bin holding the need-th largest key.
+// Thread t owns bins [NB - (t+1)B, NB - tB) with B = NB / T (>= 1); the owner
+// of the boundary hands its B bins to warp 0, which finds the bin with one
+// more warp scan. Result in sh (digit, above, cnt), after a barrier.
+template <int T, int NB>
+__device__ __forceinline__ void gfind(const uint32_t* hist, uint32_t need, GroupShared& sh,
+                                      int gtid, int bar_id) {
+  constexpr int B = NB >= T ? NB / T : 1;
+  const int lane = gtid & 31;
+  const int base = NB - (gtid + 1) * B;
+  uint32_t local = 0;
+  if (base >= 0) {
+    if constexpr (B % 4 == 0) {
+      // rotated 16-byte reads: lanes start at different 16-byte units
+#pragma unroll
+      for (int c = 0; c < B / 4; ++c) {
+        const int u = (c + lane) % (B / 4);
+        const uint4 v = *reinterpret_cast<const uint4*>(hist + base + 4 * u);
+        local += v.x + v.y + v.z + v.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < B; ++j) local += hist[base + j];
+    }
+  }
+  uint32_t tot;
+  const uint32_t excl = gscan<T>(local, &tot, sh, gtid, bar_id);
+  if (excl < need && need <= excl + local) {
+    sh.seg = static_cast<uint32_t>(gtid);
+    sh.above = excl;  // count above this thread's segment
+  }
+  group_sync<T>(bar_id);
+  if (gtid < 32) {
+    // Warp 0: the B bins of the boundary segment, one or more per lane, top first.
+    const int sbase = NB - (static_cast<int>(sh.seg) + 1) * B;
+    const uint32_t above0 = sh.above;
+    constexpr int PER = B >= 32 ? B / 32 : 1;
+    uint32_t c[PER];
+    uint32_t lsum = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int bin = sbase + B - 1 - (lane * PER + j);  // lane 0 holds the top bins
+      c[j] = (lane * PER + j < B) ? hist[bin] : 0u;
+      lsum += c[j];
+    }
+    uint32_t incl = lsum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    const uint32_t ex = above0 + incl - lsum;
+    if (ex < need && need <= ex + lsum) {
+      uint32_t run = ex;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        if (run < need && need <= run + c[j]) {
+          sh.digit = static_cast<uint32_t>(sbase + B - 1 - (lane * PER + j));
+          sh.above = run;
+          sh.cnt = c[j];
+        }
+        run += c[j];
+      }
+    }
+  }
+  group_sync<T>(bar_id);
+}
+
+// Top-k of a row whose keys[0..nb) are in shared memory (visible to the
+// group). hist: kSelHistBins words, 16-byte aligned; cand: kSelBinMax;
+// sel: min(k, nb). Writes out[0..k).
+template <int G>
+__device__ void select_row_g(const uint32_t* keys, int nb, int k, int32_t* __restrict__ out,
+                             uint32_t* hist, uint64_t* cand, uint64_t* sel, GroupShared& sh,
+                             int gtid, int bar_id) {
+  constexpr int T = 32 * G;
+  const int kk = k < nb ? k : nb;
+  enum Mode { kTakeAll, kTies, kCandidates };
+  Mode mode = kTakeAll;
+  uint32_t thr = 0, need = static_cast<uint32_t>(kk), prefix = 0;
+  int hi = 32;
+  uint32_t n_cand = 0;
+
+  if (kk > 0 && kk < nb) {
+    // ---- first digit over all keys
+    for (int i = gtid * 4; i < kSelHistBins; i += 4 * T)
+      *reinterpret_cast<uint4*>(hist + i) = make_uint4(0u, 0u, 0u, 0u);
+    group_sync<T>(bar_id);
+#pragma unroll 8
+    for (int i = gtid; i < nb; i += T) atomicAdd(&hist[keys[i] >> kSelFirstShift], 1u);
+    group_sync<T>(bar_id);
+    gfind<T, kSelHistBins>(hist, need, sh, gtid, bar_id);
+    {
+      const uint32_t digit = sh.digit, cnt = sh.cnt;
+      need -= sh.above;
+      prefix = digit << kSelFirstShift;
+      hi = kSelFirstShift;
+      if (cnt == need) {
+        mode = kTakeAll;
+        thr = prefix;
+      } else {
+        mode = kCandidates;
+        n_cand = cnt;
+      }
+    }
+    // ---- full 8-bit passes while the boundary bin is too large to compact
+    while (mode == kCandidates && n_cand > static_cast<uint32_t>(kSelBinMax)) {
+      const int nbits = hi < 8 ? hi : 8;
+      const int lo = hi - nbits;
+      const uint32_t dmask = (1u << nbits) - 1u;
+      group_sync<T>(bar_id);
+      for (int i = gtid; i < 256; i += T) hist[i] = 0;
+      group_sync<T>(bar_id);
+#pragma unroll 8
+      for (int i = gtid; i < nb; i += T) {
+        const uint32_t key = keys[i];
+        if (((key ^ prefix) >> hi) == 0) atomicAdd(&hist[(key >> lo) & dmask], 1u);
+      }
+      group_sync<T>(bar_id);
+      gfind<T, 256>(hist, need, sh, gtid, bar_id);
+      const uint32_t digit = sh.digit, cnt = sh.cnt;
+      need -= sh.above;
+      prefix |= digit << lo;
+      hi = lo;
+      if (cnt == need) {
+        mode = kTakeAll;
+        thr = prefix;
+      } else if (hi == 0) {
+        mode = kTies;
+        thr = prefix;
+      } else {
+        n_cand = cnt;
+      }
+    }
+  }
+
+  uint32_t n_win = 0;
+  if (kk > 0) {
+    // ---- gather: count, scan, write (winners -> sel, boundary keys -> cand)
+    const uint32_t bin_top = (mode == kCandidates) ? (prefix | ((1u << hi) - 1u)) : 0u;
+    uint32_t cw = 0, cc = 0;
+#pragma unroll 8
+    for (int i = gtid; i < nb; i += T) {
+      const uint32_t key = keys[i];
+      if (mode == kTakeAll) {
+        cw += key >= thr ? 1u : 0u;
+      } else if (mode == kTies) {
+        cw += key > thr ? 1u : 0u;
+      } else {
+        const bool w = key > bin_top;
+        cw += w ? 1u : 0u;
+        cc += (!w && ((key ^ prefix) >> hi) == 0) ? 1u : 0u;
+      }
+    }
+    uint32_t totals;
+    const uint32_t offs = gscan<T>((cw << 16) | cc, &totals, sh, gtid, bar_id);
+    uint32_t wo = offs >> 16, co = offs & 0xFFFFu;
+    n_win = totals >> 16;
+    if (cw | cc) {
+#pragma unroll 8
+      for (int i = gtid; i < nb; i += T) {
+        const uint32_t key = keys[i];
+        bool w, c = false;
+        if (mode == kTakeAll) {
+          w = key >= thr;
+        } else if (mode == kTies) {
+          w = key > thr;
+        } else {
+          w = key > bin_top;
+          c = !w && ((key ^ prefix) >> hi) == 0;
+        }
+        if (w) sel[wo++] = win_key(key, i);
+        if (c) cand[co++] = win_key(key, i);
+      }
+    }
+    group_sync<T>(bar_id);
+
+    if (mode == kCandidates) {
+      // ---- refine the compacted boundary keys, 8 bits at a time
+      while (n_cand > static_cast<uint32_t>(kSelRankMax) && hi > 0) {
+        const int nbits = hi < 8 ? hi : 8;
+        const int lo = hi - nbits;
+        for (int i = gtid; i < 256; i += T) hist[i] = 0;
+        group_sync<T>(bar_id);
+        for (int c = gtid; c < static_cast<int>(n_cand); c += T)
+          atomicAdd(&hist[(static_cast<uint32_t>(cand[c] >> 32) >> lo) & ((1u << nbits) - 1u)], 1u);
+        group_sync<T>(bar_id);
+        gfind<T, 256>(hist, need, sh, gtid, bar_id);
+        const uint32_t digit = sh.digit, cnt = sh.cnt;
+        const uint32_t above = sh.above;
+        const uint32_t new_prefix = prefix | (digit << lo);
+        // candidates above the new bin are winners; those in it stay
+        constexpr int kPer = (kSelBinMax + T - 1) / T;
+        uint32_t fw = 0, fc = 0;
+        uint64_t mine[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          const int c = gtid + j * T;
+          mine[j] = c < static_cast<int>(n_cand) ? cand[c] : 0ull;
+          const uint32_t d = (static_cast<uint32_t>(mine[j] >> 32) >> lo) & ((1u << nbits) - 1u);
+          fw += (c < static_cast<int>(n_cand) && d > digit) ? 1u : 0u;
+          fc += (c < static_cast<int>(n_cand) && d == digit) ? 1u : 0u;
+        }
+        uint32_t tt;
+        const uint32_t o = gscan<T>((fw << 16) | fc, &tt, sh, gtid, bar_id);  // cand reads done
+        uint32_t wo2 = n_win + (o >> 16), co2 = o & 0xFFFFu;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          const int c = gtid + j * T;
+          const uint32_t d = (static_cast<uint32_t>(mine[j] >> 32) >> lo) & ((1u << nbits) - 1u);
+          if (c < static_cast<int>(n_cand)) {
+            if (d > digit) sel[wo2++] = mine[j];
+            else if (d == digit) cand[co2++] = mine[j];
+          }
+        }
+        group_sync<T>(bar_id);
+        n_win += tt >> 16;
+        need -= above;
+        prefix = new_prefix;
+        hi = lo;
+        n_cand = cnt;
+        if (cnt == need) {
+          // every key left in the bin is a winner
+          for (int c = gtid; c < static_cast<int>(cnt); c += T) sel[n_win + c] = cand[c];
+          group_sync<T>(bar_id);
+          n_win += cnt;
+          need = 0;
+          n_cand = 0;
+          break;
+        }
+      }
+      // ---- rank the last candidates pairwise; the top `need` are winners
+      const uint32_t nd = need, nw = n_win;
+      split_rank<T>(cand, static_cast<int>(n_cand), gtid, [&](int e, uint32_t r) {
+        if (r < nd) sel[nw + r] = cand[e];
+      });
+      group_sync<T>(bar_id);
+    } else if (mode == kTies) {
+      uint32_t taken = 0;
+      for (int base = 0; base < nb && taken < need; base += T) {
+        const int i = base + gtid;
+        const bool tie = i < nb && keys[i] == thr;
+        uint32_t tot;
+        const uint32_t r = taken + gscan<T>(tie ? 1u : 0u, &tot, sh, gtid, bar_id);
+        if (tie && r < need) sel[n_win + r] = win_key(thr, i);
+        taken += tot;
+      }
+      group_sync<T>(bar_id);
+    }
+  }
+
+  // ---- output slot of every winner: its rank among the winners
   split_rank<T>(sel, kk, gtid, [&](int e, uint32_t r) {
     out[r] = static_cast<int32_t>(~static_cast<uint32_t>(sel[e]));
   });
