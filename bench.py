@@ -59,6 +59,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(qi.BY_NAME))
+    p.add_argument("--batch", type=int, default=8,
+                   help="query batches per launch for the batched measurement")
     p.add_argument("--min-timed-seconds", type=float, default=1.0,
                    help="repeat the K-step timed region until this much time has passed")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle baseline budget")
@@ -150,25 +152,27 @@ class ClockSampler:
 
 # -------------------------------------------------------------- GPU helpers
 class Sets:
-    """Rotating device buffer sets for one workload."""
+    """Rotating device buffer sets for one workload, stored as contiguous
+    [n, ...] tensors so that a slice of consecutive sets is itself a batch."""
 
     def __init__(self, torch, tbs, w, device, min_bytes):
         per = (w.nq * w.H * w.D * (4 + 2) + w.nb * w.D * 2 + w.nq * w.nb * 4 + w.nq * w.k * 4)
-        self.n = max(2, math.ceil(min_bytes / per))
+        n = max(2, math.ceil(min_bytes / per))
+        self.n = ((n + 7) // 8) * 8  # whole groups of 8 for the batched launch
         self.per_set_bytes = per
-        self.q32, self.q16, self.kb, self.scores, self.ids = [], [], [], [], []
+        self.q32 = torch.empty((self.n, w.nq, w.H, w.D), dtype=torch.float32, device=device)
+        self.kb = torch.empty((self.n, w.nb, w.D), dtype=torch.float16, device=device)
         for v in range(self.n):
             q32, _ = qi.make_f32_inputs(w, variant=v)
             _, kb = qi.make_inputs(w, variant=v)
-            self.q32.append(torch.from_numpy(q32).to(device))
-            self.kb.append(torch.from_numpy(kb).to(device))
-            self.q16.append(torch.empty((w.nq, w.H, w.D), dtype=torch.float16, device=device))
-            self.scores.append(torch.empty((w.nq, w.nb), dtype=torch.float32, device=device))
-            self.ids.append(torch.empty((w.nq, w.k), dtype=torch.int32, device=device))
+            self.q32[v].copy_(torch.from_numpy(q32))
+            self.kb[v].copy_(torch.from_numpy(kb))
+        self.q16 = torch.empty((self.n, w.nq, w.H, w.D), dtype=torch.float16, device=device)
+        self.scores = torch.empty((self.n, w.nq, w.nb), dtype=torch.float32, device=device)
+        self.ids = torch.empty((self.n, w.nq, w.k), dtype=torch.int32, device=device)
         # every q16 holds a converted copy so the score-only and select-only
         # timings read real data
-        for v in range(self.n):
-            tbs.qsa_f32_to_f16(self.q32[v], out=self.q16[v])
+        tbs.qsa_f32_to_f16(self.q32, out=self.q16)
         torch.cuda.synchronize()
 
 
@@ -268,6 +272,19 @@ def run_ours(args):
         tbs.qsa_select_step(sets.q32[v], sets.kb[v], w.n_kv, w.k, w.block,
                             scores=sets.scores[v], ids=sets.ids[v])
 
+    BB = args.batch
+
+    n_launch = (K + BB - 1) // BB
+
+    def batched(i):  # up to BB consecutive sets (one batch each) in one launch
+        nbat = min(BB, K - i * BB)
+        v = (i * BB) % sets.n
+        if v + nbat > sets.n:
+            v = 0
+        tbs.qsa_select_step_batched(sets.q32[v:v + nbat], sets.kb[v:v + nbat], w.n_kv, w.k,
+                                    w.block, scores=sets.scores[v:v + nbat],
+                                    ids=sets.ids[v:v + nbat])
+
     def score_only(i):
         v = i % sets.n
         tbs.qsa_block_scores(sets.q16[v], sets.kb[v], w.n_kv, w.block, out=sets.scores[v])
@@ -286,8 +303,9 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     # CUDA graphs of exactly K calls each (captured once, replayed)
-    graphs = {name: graph_of(torch, stream, fn, K) for name, fn in
-              (("step", step), ("score", score_only), ("select", select_only), ("convert", convert_only))}
+    graphs = {name: graph_of(torch, stream, fn, cnt) for name, fn, cnt in
+              (("step", step, K), ("score", score_only, K), ("select", select_only, K),
+               ("convert", convert_only, K), ("batched", batched, n_launch))}
     replays = {}
     for name, g in graphs.items():  # upload + one untimed replay, on the timed stream
         def rp(g=g):
@@ -310,6 +328,7 @@ def run_ours(args):
     clocks = sampler.stop()
     kern_ms = {name: statistics.median(time_region(torch, stream, replays[name], 5, 0.3))
                for name in ("score", "select", "convert")}
+    batched_ms = time_region(torch, stream, replays["batched"], 5, 0.5, barrier if dist else None)
 
     ms_step = statistics.median(step_ms) / K
     value = world * units_per_step(w) * K / (statistics.median(step_ms) / 1e3)
@@ -349,6 +368,16 @@ def run_ours(args):
         "qsa_f32_to_f16": {"us_per_launch": t["convert"] * 1e6, "gbs": bytes_convert / t["convert"] / 1e9},
     }
 
+    # the same K batches, BB per launch (qsa_select_step_batched)
+    t_b = statistics.median(batched_ms) / 1e3
+    batched_res = {
+        "batches_per_launch": BB, "launches": n_launch,
+        "value": world * units_per_step(w) * K / t_b, "unit": UNIT,
+        "ms_per_batch": t_b / K * 1e3,
+        "roofline_frac": (K * max(t_flop, t_byte)) / t_b,
+        "api": "qsa_select_step_batched (per-batch kb, CUDA graph of K/B launches)",
+    }
+
     # end-to-end through the host-buffer entry point
     e2e = run_e2e(torch, tbs, w, device, stream, K, W, barrier if dist else None)
 
@@ -365,6 +394,7 @@ def run_ours(args):
             "accumulate": "fp32"}),
         "roofline": roof,
         "separate_kernels": kernels,
+        "batched": batched_res,
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,

@@ -159,6 +159,32 @@ qsa_status qsa_select_step(const float* q32, uint16_t* q16, const uint16_t* kb, 
                            float* scores, int32_t* ids, qsa_stream_t stream);
 
 /*
+ * qsa_select_step_batched / qsa_score_select_batched - n_batches independent
+ * query batches in one launch (the selection phase's batch loop over query
+ * batches, made one launch). Batch b is exactly qsa_select_step /
+ * qsa_score_select on batch b's slices (bit-identical results):
+ *   q32 / q     f32 / f16 [n_batches, nq, H, D]; q16 (optional) likewise.
+ *   kb          f16: one [nb, D] shared by every batch when kb_batch_stride
+ *               is 0 (the block keys of one context, shared by its query
+ *               batches); otherwise batch b's [nb, D] keys start at
+ *               kb + b * kb_batch_stride (elements; a multiple of 8 and at
+ *               least nb * D).
+ *   scores      f32 [n_batches, nq, nb]; ids int32 [n_batches, nq, k].
+ * n_batches == 0 returns QSA_OK without a launch; n_batches * nq * H < 2^31.
+ * Errors as for the single-batch calls; QSA_ERR_INVALID_ARG for a negative
+ * count or stride or a stride below nb * D; QSA_ERR_MISALIGNED for a stride
+ * that is not a multiple of 8.
+ */
+qsa_status qsa_select_step_batched(const float* q32, uint16_t* q16, const uint16_t* kb,
+                                   int64_t kb_batch_stride, int32_t n_batches, int32_t nq,
+                                   int32_t H, int32_t D, int64_t n_kv, int32_t block, int32_t k,
+                                   float* scores, int32_t* ids, qsa_stream_t stream);
+qsa_status qsa_score_select_batched(const uint16_t* q, const uint16_t* kb, int64_t kb_batch_stride,
+                                    int32_t n_batches, int32_t nq, int32_t H, int32_t D,
+                                    int64_t n_kv, int32_t block, int32_t k, float* scores,
+                                    int32_t* ids, qsa_stream_t stream);
+
+/*
  * qsa_select_step_host - qsa_select_step from HOST buffers: enqueues on
  * `stream` the copies q32_host -> q32_dev and kb_host -> kb_dev, the step,
  * and the copies scores_dev -> scores_host and ids_dev -> ids_host. Host

@@ -115,6 +115,21 @@ def test_convert_and_step_reject_bad_arguments_on_host(lib):
     assert step(A + 2, A) == MISALIGNED
 
 
+def test_batched_rejects_bad_arguments_on_host(lib):
+    A = 1 << 20
+    v = ctypes.c_void_p
+    step = lambda stride, nb_: lib.qsa_select_step_batched(v(A), None, v(A), stride, nb_, 4, 8, 128,
+                                                           1000, 64, 8, v(A), v(A), None)
+    assert step(0, -1) == INVALID
+    assert step(-8, 2) == INVALID
+    assert step(8, 2) == INVALID            # stride below nb * D
+    assert step(16 * 128 + 4, 2) == MISALIGNED
+    assert step(0, 0) == OK                 # no batches: nothing to do
+    ss = lambda stride, nb_: lib.qsa_score_select_batched(v(A), v(A), stride, nb_, 4, 8, 128, 1000,
+                                                          64, 8, v(A), v(A), None)
+    assert ss(0, -1) == INVALID and ss(0, 0) == OK
+
+
 def test_selftest_rejects_bad_timeout_on_host(lib):
     assert lib.qsa_selftest_bounded_wait(0, None) == INVALID
     assert lib.qsa_selftest_bounded_wait(2_000_000_000, None) == INVALID

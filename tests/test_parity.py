@@ -164,6 +164,52 @@ def test_select_step_without_q16_output(tbs):
     assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32)) and torch.equal(a[2], b[2])
 
 
+@pytest.mark.parametrize("shared_kb", [True, False])
+@pytest.mark.parametrize("w", [qi.WORKLOADS[0], qi.WORKLOADS[2]], ids=["tiny", "mid"])
+def test_batched_step_equals_single_steps(tbs, w, shared_kb):
+    """n batches in one launch give exactly the single-batch results."""
+    B = 3
+    q32 = np.stack([qi.make_f32_inputs(w, variant=v)[0] for v in range(B)])
+    kbs = np.stack([qi.make_inputs(w, variant=v)[1] for v in range(B)])
+    kb_arg = dev(kbs[0]) if shared_kb else dev(kbs)
+    q16b, sb, ib = tbs.qsa_select_step_batched(dev(q32), kb_arg, w.n_kv, w.k, w.block,
+                                               q16=torch.empty(q32.shape, dtype=torch.float16,
+                                                               device="cuda"))
+    torch.cuda.synchronize()
+    for b in range(B):
+        kb_b = kbs[0] if shared_kb else kbs[b]
+        q16s, ss, is_ = tbs.qsa_select_step(dev(q32[b]), dev(kb_b), w.n_kv, w.k, w.block,
+                                            q16=torch.empty(q32.shape[1:], dtype=torch.float16,
+                                                            device="cuda"))
+        torch.cuda.synchronize()
+        assert torch.equal(sb[b].view(torch.int32), ss.view(torch.int32)), b
+        assert torch.equal(ib[b], is_), b
+        assert torch.equal(q16b[b].view(torch.int16), q16s.view(torch.int16)), b
+    # and batch 1 against the oracle
+    kb_1 = kbs[0] if shared_kb else kbs[1]
+    q16 = orc.f32_to_f16(q32[1])
+    s_ref, S, B_, tail = orc.reference_scores(q16, kb_1, w.n_kv, w.block)
+    s1 = sb[1].cpu().numpy()
+    assert orc.bound_report(s1, s_ref, B_)["ok"]
+    assert np.array_equal(ib[1].cpu().numpy(), orc.select_topk(s1, w.k))
+
+
+def test_batched_score_select_fp16(tbs):
+    w = qi.WORKLOADS[1]
+    B = 4
+    qs = np.stack([qi.make_inputs(w, variant=v)[0] for v in range(B)])
+    kb = qi.make_inputs(w)[1]
+    sb, ib = tbs.qsa_score_select_batched(dev(qs), dev(kb), w.n_kv, w.k, w.block)
+    torch.cuda.synchronize()
+    for b in range(B):
+        ss, is_ = tbs.qsa_score_select(dev(qs[b]), dev(kb), w.n_kv, w.k, w.block)
+        torch.cuda.synchronize()
+        assert torch.equal(sb[b].view(torch.int32), ss.view(torch.int32)), b
+        assert torch.equal(ib[b], is_), b
+    s_ref, S, B_, _ = orc.reference_scores(qs[2], kb, w.n_kv, w.block)
+    assert orc.bound_report(sb[2].cpu().numpy(), s_ref, B_)["ok"]
+
+
 def test_determinism_double_launch(tbs):
     w = qi.WORKLOADS[3]
     q, kb = qi.make_inputs(w)

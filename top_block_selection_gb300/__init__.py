@@ -17,7 +17,7 @@ __all__ = [
     "qsa_last_cuda_error", "qsa_arm",
     "qsa_num_blocks", "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select",
     "qsa_select_step", "qsa_select_step_host", "qsa_device_status", "qsa_selftest_bounded_wait",
-    "EXPORTED_SYMBOLS",
+    "qsa_select_step_batched", "qsa_score_select_batched", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -28,6 +28,7 @@ EXPORTED_SYMBOLS = (
     "qsa_abi_version", "qsa_status_str", "qsa_last_cuda_error", "qsa_arm", "qsa_num_blocks",
     "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select", "qsa_select_step",
     "qsa_select_step_host", "qsa_device_status", "qsa_selftest_bounded_wait",
+    "qsa_select_step_batched", "qsa_score_select_batched",
 )
 
 STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED_GEOMETRY",
@@ -74,6 +75,10 @@ def load_library():
                                                 vp, vp, vp, vp, vp, vp]),
         "qsa_device_status": (ctypes.c_int, [ctypes.c_int, u32p, vp]),
         "qsa_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint64, vp]),
+        "qsa_select_step_batched": (ctypes.c_int, [vp, vp, vp, i64, i32, i32, i32, i32, i64, i32,
+                                                   i32, vp, vp, vp]),
+        "qsa_score_select_batched": (ctypes.c_int, [vp, vp, i64, i32, i32, i32, i32, i64, i32, i32,
+                                                    vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -298,3 +303,77 @@ def qsa_selftest_bounded_wait(timeout_ns: int = 1_000_000, device=None):
         _check(lib.qsa_selftest_bounded_wait(timeout_ns,
                                              ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)),
                "qsa_selftest_bounded_wait")
+
+
+def _batched_kb(kb, nb, D, n_batches):
+    """(kb_batch_stride in elements) for a shared [>= nb, D] kb or a
+    per-batch [n_batches, >= nb, D] kb."""
+    torch = _torch()
+    if kb.dtype != torch.float16 or not kb.is_cuda or not kb.is_contiguous():
+        raise ValueError("kb must be a contiguous CUDA float16 tensor")
+    if kb.dim() == 2:
+        if kb.shape[1] != D or kb.shape[0] < nb:
+            raise ValueError("shared kb must be [>= nb, D]")
+        return 0
+    if kb.dim() == 3:
+        if kb.shape[0] != n_batches or kb.shape[2] != D or kb.shape[1] < nb:
+            raise ValueError("per-batch kb must be [n_batches, >= nb, D]")
+        return kb.shape[1] * D
+    raise ValueError("kb must be 2-D (shared) or 3-D (per batch)")
+
+
+def _batched_out(dev, n_batches, nq, nb, k, scores, ids):
+    torch = _torch()
+    if scores is None:
+        scores = torch.empty((n_batches, nq, nb), dtype=torch.float32, device=dev)
+    if ids is None:
+        ids = torch.empty((n_batches, nq, k), dtype=torch.int32, device=dev)
+    _need(scores, torch.float32, 3, "scores")
+    _need(ids, torch.int32, 3, "ids")
+    if tuple(scores.shape) != (n_batches, nq, nb) or tuple(ids.shape) != (n_batches, nq, k):
+        raise ValueError("scores must be [n_batches, nq, nb] and ids [n_batches, nq, k]")
+    return scores, ids
+
+
+def qsa_select_step_batched(q32, kb, n_kv: int, k: int, block: int = 64, q16=None, scores=None,
+                            ids=None):
+    """The step for q32 [n_batches, nq, H, D] in one launch; kb shared
+    ([nb, D]) or per batch ([n_batches, nb, D]). Returns (q16, scores, ids)."""
+    torch = _torch()
+    _need(q32, torch.float32, 4, "q32")
+    B, nq, H, D = q32.shape
+    nb = qsa_num_blocks(n_kv, block)
+    if nb < 0:
+        raise ValueError("n_kv must be >= 0 and block >= 1")
+    stride = _batched_kb(kb, nb, D, B)
+    scores, ids = _batched_out(q32.device, B, nq, nb, k, scores, ids)
+    if q16 is not None:
+        _need(q16, torch.float16, 4, "q16")
+        if tuple(q16.shape) != tuple(q32.shape):
+            raise ValueError("q16 must be shaped like q32")
+    lib = load_library()
+    with torch.cuda.device(q32.device):
+        _check(lib.qsa_select_step_batched(_ptr(q32), _ptr(q16) if q16 is not None else None,
+                                           _ptr(kb), stride, B, nq, H, D, n_kv, block, k,
+                                           _ptr(scores), _ptr(ids), _stream_of(q32)),
+               "qsa_select_step_batched")
+    return q16, scores, ids
+
+
+def qsa_score_select_batched(q, kb, n_kv: int, k: int, block: int = 64, scores=None, ids=None):
+    """Scores and top-k for fp16 q [n_batches, nq, H, D] in one launch; kb
+    shared or per batch as for qsa_select_step_batched."""
+    torch = _torch()
+    _need(q, torch.float16, 4, "q")
+    B, nq, H, D = q.shape
+    nb = qsa_num_blocks(n_kv, block)
+    if nb < 0:
+        raise ValueError("n_kv must be >= 0 and block >= 1")
+    stride = _batched_kb(kb, nb, D, B)
+    scores, ids = _batched_out(q.device, B, nq, nb, k, scores, ids)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        _check(lib.qsa_score_select_batched(_ptr(q), _ptr(kb), stride, B, nq, H, D, n_kv, block, k,
+                                            _ptr(scores), _ptr(ids), _stream_of(q)),
+               "qsa_score_select_batched")
+    return scores, ids

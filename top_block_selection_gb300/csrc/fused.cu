@@ -58,6 +58,9 @@ struct FusedArgs {
   float* scores;        // [nq, nb]
   int32_t* ids;         // [nq, k]
   int32_t nq, D, nb, n_full, has_tail, k;
+  int32_t groups_per_batch;  // query groups of one batch; blocks are (batch, group, rank)
+  int64_t q_batch_elems;     // nq * H * D: q32 / q16 / q16out elements per batch
+  int64_t kb_batch_stride;   // kb elements between batches; 0 = one kb shared by all
   int32_t bn, qg, m_tiles, n_chunks, k_steps;
   uint32_t tmem_cols;
   uint32_t sel_bytes;   // shared bytes of one select group (cand + sel, plus keys +
@@ -150,13 +153,23 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = static_cast<int>(cluster_rank());
-  const int group = blockIdx.x / kCluster;
-  const int q0 = group * a.qg;                 // first query of the group
+  const int cluster_id = blockIdx.x / kCluster;
+  const int batch = cluster_id / a.groups_per_batch;
+  const int group = cluster_id - batch * a.groups_per_batch;
+  const int q0 = group * a.qg;                 // first query of the group (in its batch)
+  // this block's batch: its slices of every tensor
+  const float* q32b = kF32Q ? a.q32 + batch * a.q_batch_elems : nullptr;
+  __half* q16outb = a.q16out != nullptr ? a.q16out + batch * a.q_batch_elems : nullptr;
+  const __half* kbb = a.kb + batch * a.kb_batch_stride;
+  float* scoresb = a.scores + static_cast<int64_t>(batch) * a.nq * a.nb;
+  int32_t* idsb = a.ids + static_cast<int64_t>(batch) * a.nq * a.k;
+  const int kb_z = a.kb_batch_stride != 0 ? batch : 0;  // kb tensor map: 3rd coordinate
+  const int q_row0 = batch * a.nq * H;                  // fp16 q tensor map: batch row offset
   const int col0 = q0 * H;                     // first row of the [nq*H, D] query view
   const int qh_rows = min(a.bn, (a.nq - q0) * H);
   const int n_local = a.m_tiles > rank ? (a.m_tiles - rank + kCluster - 1) / kCluster : 0;
   const bool tail_owner = a.has_tail && rank == kCluster - 1;
-  const bool need_q = n_local > 0 || tail_owner || (kF32Q && a.q16out != nullptr && rank == 0);
+  const bool need_q = n_local > 0 || tail_owner || (kF32Q && q16outb != nullptr && rank == 0);
   const int rows_here = a.qg > rank ? (a.qg - rank + kCluster - 1) / kCluster : 0;
   const uint32_t rows_base = smem_u32(smem + a.rows_off);
   const bool producer_warp = warp == kProducerWarp;
@@ -183,14 +196,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
     if (!kF32Q && need_q) {
       mbar_arrive_expect_tx(&bar_q, static_cast<uint32_t>(a.n_chunks * a.bn * kFRowBytes));
       for (int c = 0; c < a.n_chunks; ++c)
-        tma_load_2d(sQ + c * a.bn * kFRowBytes, &tm_q, c * kFKAtom, col0, &bar_q);
+        tma_load_2d(sQ + c * a.bn * kFRowBytes, &tm_q, c * kFKAtom, q_row0 + col0, &bar_q);
     }
     for (int t = 0; t < 2 && t < n_local; ++t) {
       const int m = rank + t * kCluster;
       mbar_arrive_expect_tx(&bar_full[t], static_cast<uint32_t>(stage_bytes));
       for (int c = 0; c < a.n_chunks; ++c)
-        tma_load_2d(sKB + t * stage_bytes + c * kFTileM * kFRowBytes, &tm_kb, c * kFKAtom,
-                    m * kFTileM, &bar_full[t]);
+        tma_load_3d(sKB + t * stage_bytes + c * kFTileM * kFRowBytes, &tm_kb, c * kFKAtom,
+                    m * kFTileM, kb_z, &bar_full[t]);
     }
   }
   // DSMEM mode: peers store into this CTA's shared memory only after every
@@ -216,7 +229,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
         const int i = (f - row * f4_per_row) * 4;
         v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (f < total && row < qh_rows && i < a.D)
-          v[j] = __ldg(reinterpret_cast<const float4*>(a.q32 + static_cast<int64_t>(col0 + row) * a.D + i));
+          v[j] = __ldg(reinterpret_cast<const float4*>(q32b + static_cast<int64_t>(col0 + row) * a.D + i));
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -230,8 +243,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
           pk.x = *reinterpret_cast<const uint32_t*>(&h01);
           pk.y = *reinterpret_cast<const uint32_t*>(&h23);
           *reinterpret_cast<uint2*>(sQ + sw128_offset(a.bn, row, i)) = pk;
-          if (a.q16out != nullptr && rank == 0 && row < qh_rows && i < a.D)
-            *reinterpret_cast<uint2*>(a.q16out + static_cast<int64_t>(col0 + row) * a.D + i) = pk;
+          if (q16outb != nullptr && rank == 0 && row < qh_rows && i < a.D)
+            *reinterpret_cast<uint2*>(q16outb + static_cast<int64_t>(col0 + row) * a.D + i) = pk;
         }
       }
     }
@@ -272,8 +285,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
           const int m = rank + (t + 2) * kCluster;
           mbar_arrive_expect_tx(&bar_full[s], static_cast<uint32_t>(stage_bytes));
           for (int c = 0; c < a.n_chunks; ++c)
-            tma_load_2d(sKB + s * stage_bytes + c * kFTileM * kFRowBytes, &tm_kb, c * kFKAtom,
-                        m * kFTileM, &bar_full[s]);
+            tma_load_3d(sKB + s * stage_bytes + c * kFTileM * kFRowBytes, &tm_kb, c * kFKAtom,
+                        m * kFTileM, kb_z, &bar_full[s]);
         }
       }
       if (!ok) {
@@ -302,7 +315,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
         atomicOr(a.status, kErrScoreLoadTimeout);
       }
       const int pairs = qh_rows;
-      const __half* krow = a.kb + static_cast<int64_t>(a.nb - 1) * a.D;
+      const __half* krow = kbb + static_cast<int64_t>(a.nb - 1) * a.D;
       for (int p = tid; p < pairs; p += 128) {
         float acc = 0.0f;
         for (int i = 0; i < a.D; i += 8) {
@@ -326,7 +339,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
 #pragma unroll
         for (int h = 0; h < H; ++h) s = __fadd_rn(s, fmaxf(tail_acc[ql * H + h], 0.0f));
         const float score = __fadd_rn(s, 1.0e9f);
-        a.scores[static_cast<int64_t>(q0 + ql) * a.nb + (a.nb - 1)] = score;
+        scoresb[static_cast<int64_t>(q0 + ql) * a.nb + (a.nb - 1)] = score;
         if (a.dsmem) send_key(rows_base, a.row_bytes, ql, a.nb - 1, score);
       }
     }
@@ -352,7 +365,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
       if (failed) break;
       const int b = (rank + t * kCluster) * kFTileM + quarter * 32 + lane;
       const bool b_ok = b < a.n_full;
-      float* out = a.scores + b;
+      float* out = scoresb + b;
       const uint32_t taddr =
           tmem_base + static_cast<uint32_t>(s * a.bn) + (static_cast<uint32_t>(quarter * 32) << 16);
       constexpr int kQPerLoad = 32 / H;
@@ -398,8 +411,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
   for (int r = 0; r < rows_here; ++r) {
     const int qi = q0 + rank + r * kCluster;
     if (qi >= a.nq) break;
-    int32_t* out = a.ids + static_cast<int64_t>(qi) * a.k;
-    const float* row = a.scores + static_cast<int64_t>(qi) * a.nb;
+    int32_t* out = idsb + static_cast<int64_t>(qi) * a.k;
+    const float* row = scoresb + static_cast<int64_t>(qi) * a.nb;
     const uint32_t* rk = reinterpret_cast<const uint32_t*>(smem + a.rows_off + r * a.row_bytes);
     if (a.nb <= 8 * kWork) {
       uint32_t key[8];
@@ -456,6 +469,20 @@ const void* fused_kernel_for(int H, bool f32q) {
   }
 }
 
+// 3-D fp16 map: [z][rows][cols] with a z stride in elements (a multiple of 8).
+bool encode_f16_3d(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint64_t zs,
+                   uint64_t z_stride, uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {cols, rows, zs};
+  const cuuint64_t strides[2] = {cols * 2, z_stride * 2};
+  const cuuint32_t box[3] = {box_cols, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_f16_2d(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows,
                    uint32_t box_cols, uint32_t box_rows) {
   EncodeTiledFn enc = encode_tiled_fn();
@@ -499,7 +526,8 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
   }
   const int qg = bn / p.H;
   const int64_t groups = (p.nq + qg - 1) / qg;
-  if (groups * kCluster > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  const int64_t blocks = static_cast<int64_t>(p.n_batches) * groups * kCluster;
+  if (blocks > 0x7FFFFFFFLL || groups > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   FusedArgs a;
   a.q32 = p.q32;
   a.q16in = reinterpret_cast<const __half*>(p.q16);
@@ -508,6 +536,9 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
   a.scores = p.scores;
   a.ids = p.ids;
   a.nq = p.nq;
+  a.groups_per_batch = static_cast<int32_t>(groups);
+  a.q_batch_elems = static_cast<int64_t>(p.nq) * p.H * p.D;
+  a.kb_batch_stride = p.kb_batch_stride;
   a.D = p.D;
   a.nb = static_cast<int32_t>(p.nb);
   a.n_full = static_cast<int32_t>(p.n_full);
@@ -544,16 +575,21 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
   CUtensorMap tm_kb, tm_q;
   memset(&tm_kb, 0, sizeof(tm_kb));
   memset(&tm_q, 0, sizeof(tm_q));
-  if (p.n_full > 0 && !encode_f16_2d(&tm_kb, p.kb, p.D, p.n_full, kFKAtom, kFTileM))
-    return cudaErrorInvalidValue;
+  if (p.n_full > 0) {
+    const uint64_t zs = p.kb_batch_stride != 0 ? static_cast<uint64_t>(p.n_batches) : 1u;
+    const uint64_t zst = p.kb_batch_stride != 0 ? static_cast<uint64_t>(p.kb_batch_stride)
+                                                : static_cast<uint64_t>(p.n_full) * p.D;
+    if (!encode_f16_3d(&tm_kb, p.kb, p.D, p.n_full, zs, zst, kFKAtom, kFTileM))
+      return cudaErrorInvalidValue;
+  }
   if (p.q32 == nullptr &&
-      !encode_f16_2d(&tm_q, p.q16, p.D, static_cast<uint64_t>(p.nq) * p.H, kFKAtom, bn))
+      !encode_f16_2d(&tm_q, p.q16, p.D, static_cast<uint64_t>(p.n_batches) * p.nq * p.H, kFKAtom, bn))
     return cudaErrorInvalidValue;
   const bool f32q = p.q32 != nullptr;
   const void* fn = fused_kernel_for(p.H, f32q);
   if (fn == nullptr) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(groups * kCluster));
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kFThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

@@ -152,7 +152,8 @@ qsa_status qsa_score_select(const uint16_t* q, const uint16_t* kb, int32_t nq, i
   if (g.nb > 0 && (!q || !kb)) return QSA_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
-  qsa::FusedProblem p{nullptr, q, nullptr, kb, scores, ids, nq, H, D, g.nb, g.n_full, g.has_tail, k};
+  qsa::FusedProblem p{nullptr, q,       nullptr,  kb, scores, ids, nq, H, D, g.nb, g.n_full,
+                      g.has_tail, k, 1, 0};
   return from_cuda(qsa::launch_fused(p, *dev, as_cuda(stream)));
 }
 
@@ -170,7 +171,56 @@ qsa_status qsa_select_step(const float* q32, uint16_t* q16, const uint16_t* kb, 
   if (!aligned(q32, 16) || !aligned(q16, 16)) return QSA_ERR_MISALIGNED;
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
-  qsa::FusedProblem p{q32, nullptr, q16, kb, scores, ids, nq, H, D, g.nb, g.n_full, g.has_tail, k};
+  qsa::FusedProblem p{q32, nullptr, q16, kb, scores, ids, nq, H, D, g.nb, g.n_full,
+                      g.has_tail, k, 1, 0};
+  return from_cuda(qsa::launch_fused(p, *dev, as_cuda(stream)));
+}
+
+// Shared by the two batched entry points: batch count and kb stride rules.
+static qsa_status check_batches(int32_t n_batches, int64_t kb_batch_stride, int64_t nb, int32_t D) {
+  if (n_batches < 0 || kb_batch_stride < 0) return QSA_ERR_INVALID_ARG;
+  if (kb_batch_stride != 0 && kb_batch_stride < nb * D) return QSA_ERR_INVALID_ARG;
+  if (kb_batch_stride % 8 != 0) return QSA_ERR_MISALIGNED;
+  return QSA_OK;
+}
+
+qsa_status qsa_score_select_batched(const uint16_t* q, const uint16_t* kb, int64_t kb_batch_stride,
+                                    int32_t n_batches, int32_t nq, int32_t H, int32_t D,
+                                    int64_t n_kv, int32_t block, int32_t k, float* scores,
+                                    int32_t* ids, qsa_stream_t stream) {
+  Geometry g;
+  qsa_status st = check_scores(q, kb, nq, H, D, n_kv, block, scores, &g);
+  if (st != QSA_OK) return st;
+  if ((st = check_select(scores, nq, g.nb, k, ids)) != QSA_OK) return st;
+  if ((st = check_batches(n_batches, kb_batch_stride, g.nb, D)) != QSA_OK) return st;
+  if (nq == 0 || n_batches == 0) return QSA_OK;
+  if (static_cast<int64_t>(n_batches) * nq * H > 0x7FFFFFFFLL) return QSA_ERR_UNSUPPORTED_GEOMETRY;
+  if (g.nb > 0 && (!q || !kb)) return QSA_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  qsa::FusedProblem p{nullptr, q,       nullptr,  kb, scores, ids, nq, H, D, g.nb, g.n_full,
+                      g.has_tail, k, n_batches, kb_batch_stride};
+  return from_cuda(qsa::launch_fused(p, *dev, as_cuda(stream)));
+}
+
+qsa_status qsa_select_step_batched(const float* q32, uint16_t* q16, const uint16_t* kb,
+                                   int64_t kb_batch_stride, int32_t n_batches, int32_t nq,
+                                   int32_t H, int32_t D, int64_t n_kv, int32_t block, int32_t k,
+                                   float* scores, int32_t* ids, qsa_stream_t stream) {
+  Geometry g;
+  qsa_status st = check_scores(reinterpret_cast<const uint16_t*>(q32), kb, nq, H, D, n_kv, block,
+                               scores, &g);
+  if (st != QSA_OK) return st;
+  if ((st = check_select(scores, nq, g.nb, k, ids)) != QSA_OK) return st;
+  if ((st = check_batches(n_batches, kb_batch_stride, g.nb, D)) != QSA_OK) return st;
+  if (nq == 0 || n_batches == 0) return QSA_OK;
+  if (static_cast<int64_t>(n_batches) * nq * H > 0x7FFFFFFFLL) return QSA_ERR_UNSUPPORTED_GEOMETRY;
+  if (!q32) return QSA_ERR_INVALID_ARG;
+  if (!aligned(q32, 16) || !aligned(q16, 16)) return QSA_ERR_MISALIGNED;
+  const DeviceInfo* dev = nullptr;
+  if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  qsa::FusedProblem p{q32, nullptr, q16, kb, scores, ids, nq, H, D, g.nb, g.n_full,
+                      g.has_tail, k, n_batches, kb_batch_stride};
   return from_cuda(qsa::launch_fused(p, *dev, as_cuda(stream)));
 }
 

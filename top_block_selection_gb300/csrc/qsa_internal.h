@@ -63,6 +63,8 @@ struct FusedProblem {
   int64_t nb, n_full;
   bool has_tail;
   int32_t k;
+  int32_t n_batches;        // independent query batches in this launch (>= 1)
+  int64_t kb_batch_stride;  // kb elements between batches; 0 = kb shared by all batches
 };
 cudaError_t init_fused_kernels(const DeviceInfo& dev);
 cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStream_t stream);
