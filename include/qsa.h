@@ -134,10 +134,13 @@ qsa_status qsa_select(const float* scores, int32_t nq, int32_t nb, int32_t k, in
                       qsa_stream_t stream);
 
 /*
- * qsa_score_select - the metric path in one launch: the results of
- * qsa_block_scores and then qsa_select, with the same arguments and rules as
- * those two (and bit-identical results). Both outputs are written: scores
- * [nq, nb] and ids [nq, k].
+ * qsa_score_select - the metric path: the results of qsa_block_scores and
+ * then qsa_select, with the same arguments and rules as those two (and
+ * bit-identical results). Both outputs are written: scores [nq, nb] and ids
+ * [nq, k]. Up to a few waves of work this is one fused launch; a larger
+ * problem (more than eight fused CTAs per SM, e.g. 4096 queries of 16 heads)
+ * runs the score, tail and select kernels in turn instead, chained by
+ * programmatic dependent launch. The results are the same bits either way.
  */
 qsa_status qsa_score_select(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H,
                             int32_t D, int64_t n_kv, int32_t block, int32_t k, float* scores,
@@ -153,16 +156,31 @@ qsa_status qsa_score_select(const uint16_t* q, const uint16_t* kb, int32_t nq, i
  *   q16  optional: NULL, or f16 [nq, H, D] device, 16-byte aligned, which
  *        then receives the converted queries.
  *   The other arguments as for qsa_score_select.
+ * A problem too large for the fused launch (as for qsa_score_select) runs
+ * the conversion into q16 and then the separate kernels when q16 is given,
+ * and the fused launch when it is NULL (no buffer for the fp16 operand).
  */
 qsa_status qsa_select_step(const float* q32, uint16_t* q16, const uint16_t* kb, int32_t nq,
                            int32_t H, int32_t D, int64_t n_kv, int32_t block, int32_t k,
                            float* scores, int32_t* ids, qsa_stream_t stream);
 
 /*
+ * qsa_select_step_launches - the number of kernel launches one call of
+ * qsa_select_step with these sizes makes on the current device: 1 for the
+ * fused launch, more for the separate kernels, 0 when there is nothing to
+ * compute (nq == 0 or nb == 0). with_q16 says whether the call passes a q16
+ * buffer. Returns -1 for sizes qsa_select_step would reject or when the
+ * current device cannot run the library. Launches nothing.
+ */
+int32_t qsa_select_step_launches(int32_t nq, int32_t H, int32_t D, int64_t n_kv, int32_t block,
+                                 int32_t k, int32_t with_q16);
+
+/*
  * qsa_select_step_batched / qsa_score_select_batched - n_batches independent
  * query batches in one launch (the selection phase's batch loop over query
  * batches, made one launch). Batch b is exactly qsa_select_step /
- * qsa_score_select on batch b's slices (bit-identical results):
+ * qsa_score_select on batch b's slices (bit-identical results), and always
+ * one fused launch whatever the size:
  *   q32 / q     f32 / f16 [n_batches, nq, H, D]; q16 (optional) likewise.
  *   kb          f16: one [nb, D] shared by every batch when kb_batch_stride
  *               is 0 (the block keys of one context, shared by its query

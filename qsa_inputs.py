@@ -56,7 +56,14 @@ WORKLOADS = [
     Workload("prefill_nq4096_h16_d128_kv131073", 4096, 16, 128, 131072 + 1, 64, 64, "normal_d_onehot", 1005),
 ]
 
-BY_NAME = {w.name: w for w in WORKLOADS}
+# Decode-shaped batches (few queries against a long context), same recipe.
+DECODE_WORKLOADS = [
+    Workload("decode_nq1_h8_d128_kv131072", 1, 8, 128, 131072, 64, 64, "normal_d", 1101),
+    Workload("decode_nq4_h8_d128_kv131072", 4, 8, 128, 131072, 64, 64, "normal_d", 1102),
+    Workload("decode_nq16_h8_d128_kv131072", 16, 8, 128, 131072, 64, 64, "normal_d", 1103),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + DECODE_WORKLOADS}
 
 
 def _f16(x: np.ndarray) -> np.ndarray:

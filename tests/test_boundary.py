@@ -130,6 +130,17 @@ def test_batched_rejects_bad_arguments_on_host(lib):
     assert ss(0, -1) == INVALID and ss(0, 0) == OK
 
 
+def test_step_launches_host_rules(lib):
+    n = lambda nq, H, D, n_kv, block, k, q16: lib.qsa_select_step_launches(nq, H, D, n_kv, block, k, q16)
+    assert n(4, 3, 128, 1000, 64, 8, 1) == -1        # unsupported head count
+    assert n(4, 8, 120, 1000, 64, 8, 1) == -1        # D not a multiple of 16
+    assert n(4, 8, 128, 1000, 64, 2000, 1) == -1     # k above the select limit
+    assert n(4, 8, 128, 64 * 40000, 64, 8, 1) == -1  # nb above the select limit
+    assert n(-1, 8, 128, 1000, 64, 8, 1) == -1
+    assert n(0, 8, 128, 1000, 64, 8, 1) == 0         # nothing to compute
+    assert n(4, 8, 128, 0, 64, 8, 1) == 0
+
+
 def test_selftest_rejects_bad_timeout_on_host(lib):
     assert lib.qsa_selftest_bounded_wait(0, None) == INVALID
     assert lib.qsa_selftest_bounded_wait(2_000_000_000, None) == INVALID

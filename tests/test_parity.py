@@ -63,6 +63,19 @@ def test_workload_parity(tbs, w):
           f"guarded rows {sel['guarded_rows']}, exact rows {sel['exact_rows']}")
 
 
+@pytest.mark.parametrize("w", qi.DECODE_WORKLOADS, ids=[w.name for w in qi.DECODE_WORKLOADS])
+def test_decode_shapes(tbs, w):
+    q, kb = qi.make_inputs(w)
+    check_case(tbs, q, kb, w.n_kv, w.block, w.k, w.name)
+    q32, _ = qi.make_f32_inputs(w)
+    _, s_gpu, ids_gpu = tbs.qsa_select_step(dev(q32), dev(kb), w.n_kv, w.k, w.block)
+    torch.cuda.synchronize()
+    s = s_gpu.cpu().numpy()
+    s_ref, S, B, _ = orc.reference_scores(orc.f32_to_f16(q32), kb, w.n_kv, w.block)
+    assert orc.bound_report(s, s_ref, B)["ok"]
+    assert np.array_equal(ids_gpu.cpu().numpy(), orc.select_topk(s, w.k))
+
+
 @pytest.mark.parametrize("H", [1, 2, 4, 8, 16, 32])
 @pytest.mark.parametrize("D", [16, 64, 80, 128, 256])
 def test_coordinate_coded_exact(tbs, H, D):
@@ -150,6 +163,31 @@ def test_fused_matches_separate_kernels(tbs):
         torch.cuda.synchronize()
         assert torch.equal(s_f.view(torch.int32), s_u.view(torch.int32)), w.name
         assert torch.equal(i_f, i_u), w.name
+
+
+def test_large_step_paths_agree(tbs):
+    """On the 4096-query prefill shape the single-batch entry points run the
+    separate stages (convert, score + tail, select) and the batched entry
+    points the one fused kernel; both give the same bits."""
+    w = qi.BY_NAME["prefill_nq4096_h16_d128_kv131073"]
+    q32, _ = qi.make_f32_inputs(w)
+    _, kb = qi.make_inputs(w)
+    kd = dev(kb)
+    q16_buf = torch.empty(q32.shape, dtype=torch.float16, device="cuda")
+    q16_s, s_s, i_s = tbs.qsa_select_step(dev(q32), kd, w.n_kv, w.k, w.block, q16=q16_buf)
+    _, s_f, i_f = tbs.qsa_select_step(dev(q32), kd, w.n_kv, w.k, w.block)
+    s_b, i_b = tbs.qsa_score_select_batched(q16_s[None], kd, w.n_kv, w.k, w.block)
+    s_1, i_1 = tbs.qsa_score_select(q16_s, kd, w.n_kv, w.k, w.block)
+    torch.cuda.synchronize()
+    for s, i in ((s_f, i_f), (s_b[0], i_b[0]), (s_1, i_1)):
+        assert torch.equal(s.view(torch.int32), s_s.view(torch.int32))
+        assert torch.equal(i, i_s)
+    assert np.array_equal(q16_s.cpu().numpy().view(np.uint16), orc.f32_to_f16(q32).view(np.uint16))
+    # the launch plan the library reports for the two calls
+    assert tbs.qsa_select_step_launches(w.nq, w.H, w.D, w.n_kv, w.k, w.block, with_q16=True) == 4
+    assert tbs.qsa_select_step_launches(w.nq, w.H, w.D, w.n_kv, w.k, w.block, with_q16=False) == 1
+    h = qi.BY_NAME["long128k_nq256_h8_d128_kv131072"]
+    assert tbs.qsa_select_step_launches(h.nq, h.H, h.D, h.n_kv, h.k, h.block, with_q16=True) == 1
 
 
 def test_select_step_without_q16_output(tbs):

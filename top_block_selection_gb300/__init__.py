@@ -17,7 +17,8 @@ __all__ = [
     "qsa_last_cuda_error", "qsa_arm",
     "qsa_num_blocks", "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select",
     "qsa_select_step", "qsa_select_step_host", "qsa_device_status", "qsa_selftest_bounded_wait",
-    "qsa_select_step_batched", "qsa_score_select_batched", "EXPORTED_SYMBOLS",
+    "qsa_select_step_batched", "qsa_score_select_batched", "qsa_select_step_launches",
+    "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -28,7 +29,7 @@ EXPORTED_SYMBOLS = (
     "qsa_abi_version", "qsa_status_str", "qsa_last_cuda_error", "qsa_arm", "qsa_num_blocks",
     "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select", "qsa_select_step",
     "qsa_select_step_host", "qsa_device_status", "qsa_selftest_bounded_wait",
-    "qsa_select_step_batched", "qsa_score_select_batched",
+    "qsa_select_step_batched", "qsa_score_select_batched", "qsa_select_step_launches",
 )
 
 STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED_GEOMETRY",
@@ -79,6 +80,7 @@ def load_library():
                                                    i32, vp, vp, vp]),
         "qsa_score_select_batched": (ctypes.c_int, [vp, vp, i64, i32, i32, i32, i32, i64, i32, i32,
                                                     vp, vp, vp]),
+        "qsa_select_step_launches": (i32, [i32, i32, i32, i64, i32, i32, i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -303,6 +305,20 @@ def qsa_selftest_bounded_wait(timeout_ns: int = 1_000_000, device=None):
         _check(lib.qsa_selftest_bounded_wait(timeout_ns,
                                              ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)),
                "qsa_selftest_bounded_wait")
+
+
+def qsa_select_step_launches(nq: int, H: int, D: int, n_kv: int, k: int, block: int = 64,
+                             with_q16: bool = True, device=None) -> int:
+    """Kernel launches one qsa_select_step call of these sizes makes on the
+    device (1 = the fused launch); raises for sizes the step rejects."""
+    torch = _torch()
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        n = int(lib.qsa_select_step_launches(nq, H, D, n_kv, block, k, 1 if with_q16 else 0))
+    if n < 0:
+        raise QsaError(1, "qsa_select_step_launches")
+    return n
 
 
 def _batched_kb(kb, nb, D, n_batches):

@@ -15,6 +15,8 @@ constexpr int kConvThreads = 256;
 
 __global__ void __launch_bounds__(kConvThreads)
     convert_vec8_kernel(const float4* __restrict__ src, uint4* __restrict__ dst, int64_t n8) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
        i += stride) {
@@ -35,6 +37,8 @@ __global__ void __launch_bounds__(kConvThreads)
 
 __global__ void __launch_bounds__(kConvThreads)
     convert_scalar_kernel(const float* __restrict__ src, __half* __restrict__ dst, int64_t n) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += stride)
@@ -53,9 +57,10 @@ cudaError_t launch_convert(const float* src, uint16_t* dst, int64_t n, const Dev
     if (n8 > 0) {
       int64_t blocks = (n8 + kConvThreads - 1) / kConvThreads;
       if (blocks > wave * 4) blocks = wave * 4;
-      convert_vec8_kernel<<<static_cast<unsigned>(blocks), kConvThreads, 0, stream>>>(
-          reinterpret_cast<const float4*>(src), reinterpret_cast<uint4*>(dst), n8);
-      cudaError_t e = cudaGetLastError();
+      cudaError_t e = launch_pdl(convert_vec8_kernel, dim3(static_cast<unsigned>(blocks)),
+                                 dim3(kConvThreads), 0, stream,
+                                 reinterpret_cast<const float4*>(src), reinterpret_cast<uint4*>(dst),
+                                 n8);
       if (e != cudaSuccess) return e;
     }
     done = n8 * 8;
@@ -64,9 +69,8 @@ cudaError_t launch_convert(const float* src, uint16_t* dst, int64_t n, const Dev
   if (rest > 0) {
     int64_t blocks = (rest + kConvThreads - 1) / kConvThreads;
     if (blocks > wave * 4) blocks = wave * 4;
-    convert_scalar_kernel<<<static_cast<unsigned>(blocks), kConvThreads, 0, stream>>>(
-        src + done, reinterpret_cast<__half*>(dst) + done, rest);
-    return cudaGetLastError();
+    return launch_pdl(convert_scalar_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kConvThreads),
+                      0, stream, src + done, reinterpret_cast<__half*>(dst) + done, rest);
   }
   return cudaSuccess;
 }

@@ -176,8 +176,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
 
   // Programmatic dependent launch: the next kernel on the stream may start its
   // own set-up now; this kernel reads nothing produced by earlier work on the
-  // stream before griddepcontrol.wait below.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // stream before pdl_wait() below.
+  pdl_launch_dependents();
   if (tid == kProducerWarp * 32) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_full[s], 1);
@@ -191,7 +191,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
     if (n_local > 0) tma_prefetch_desc(&tm_kb);
     if (!kF32Q && need_q) tma_prefetch_desc(&tm_q);
   }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();
   if (tid == kProducerWarp * 32) {
     if (!kF32Q && need_q) {
       mbar_arrive_expect_tx(&bar_q, static_cast<uint32_t>(a.n_chunks * a.bn * kFRowBytes));
@@ -211,10 +211,12 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
   if (a.dsmem) cluster_arrive_release();
   __syncwarp();
   if (producer_warp) {
-    if (n_local > 0) {
-      tmem_alloc(&tmem_slot, a.tmem_cols);
-      tmem_relinquish();
-    }
+    if (n_local > 0) tmem_alloc(&tmem_slot, a.tmem_cols);
+    // Every CTA gives up its TMEM allocation permit, also one that allocates
+    // nothing: a CTA still holding the permit kept the SM from taking
+    // another CTA (measured: ranks without tiles halved the resident
+    // clusters).
+    tmem_relinquish();
   } else if (kF32Q && need_q) {
     // fp32 queries -> fp16 (round to nearest even) -> swizzled operand tile,
     // by the kWork threads. Rows past the last query and columns past D are 0.
@@ -510,20 +512,34 @@ cudaError_t init_fused_kernels(const DeviceInfo& dev) {
       e = cudaFuncSetAttribute(fused_kernel_for(H, f), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dev.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
       if (e != cudaSuccess) return e;
+      // Always the largest shared-memory carveout: two CTAs of a cluster per
+      // SM need it, and a smaller carveout chosen from one launch's request
+      // left room for one cluster CTA per SM (half the clusters resident).
+      e = cudaFuncSetAttribute(fused_kernel_for(H, f),
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return e;
     }
   return cudaSuccess;
 }
 
+namespace {
+// Columns per query group: 64 unless that would need more than about two
+// waves of 8-CTA clusters, then 128.
+int fused_bn(int32_t nq, int32_t H, const DeviceInfo& dev) {
+  const int64_t groups64 = (nq + (64 / std::min(64, H)) - 1) / (64 / std::min(64, H));
+  return groups64 * kCluster > 4LL * dev.sm_count ? 128 : std::max(64, static_cast<int>(H));
+}
+}  // namespace
+
+int64_t fused_blocks(int32_t nq, int32_t H, const DeviceInfo& dev) {
+  const int qg = fused_bn(nq, H, dev) / H;
+  return ((static_cast<int64_t>(nq) + qg - 1) / qg) * kCluster;
+}
+
 cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStream_t stream) {
   if (p.nq <= 0) return cudaSuccess;
-  // Columns per group: 64 unless that would need more than about two waves
-  // of 8-CTA clusters, then 128.
-  int bn = 64;
-  if (bn < p.H) bn = p.H;
-  {
-    const int64_t groups64 = (p.nq + (64 / std::min(64, p.H)) - 1) / (64 / std::min(64, p.H));
-    if (groups64 * kCluster > 4LL * dev.sm_count) bn = 128;
-  }
+  const int bn = fused_bn(p.nq, p.H, dev);
   const int qg = bn / p.H;
   const int64_t groups = (p.nq + qg - 1) / qg;
   const int64_t blocks = static_cast<int64_t>(p.n_batches) * groups * kCluster;

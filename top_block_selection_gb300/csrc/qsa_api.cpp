@@ -78,6 +78,24 @@ qsa_status run_scores(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t
   return from_cuda(qsa::launch_scores(p, dev, stream));
 }
 
+// The single-batch steps run either the one fused cluster kernel or the
+// separate stages (convert, score + tail, select) chained by programmatic
+// dependent launch. Fused wins while its CTAs fit in a few waves (it saves the
+// scores round trip and the launch gaps); past that the separate score kernel,
+// which tiles 128 key blocks per MMA against many queries, does less work per
+// score. Both write identical scores and ids.
+bool use_separate(int32_t nq, int32_t H, const DeviceInfo& dev) {
+  return qsa::fused_blocks(nq, H, dev) > 8LL * dev.sm_count;
+}
+
+qsa_status run_separate(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H, int32_t D,
+                        const Geometry& g, int32_t k, float* scores, int32_t* ids,
+                        const DeviceInfo& dev, cudaStream_t stream) {
+  qsa_status st = run_scores(q, kb, nq, H, D, g, scores, dev, stream);
+  if (st != QSA_OK) return st;
+  return from_cuda(qsa::launch_select(scores, nq, static_cast<int32_t>(g.nb), k, ids, dev, stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -152,6 +170,8 @@ qsa_status qsa_score_select(const uint16_t* q, const uint16_t* kb, int32_t nq, i
   if (g.nb > 0 && (!q || !kb)) return QSA_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  if (g.nb > 0 && use_separate(nq, H, *dev))
+    return run_separate(q, kb, nq, H, D, g, k, scores, ids, *dev, as_cuda(stream));
   qsa::FusedProblem p{nullptr, q,       nullptr,  kb, scores, ids, nq, H, D, g.nb, g.n_full,
                       g.has_tail, k, 1, 0};
   return from_cuda(qsa::launch_fused(p, *dev, as_cuda(stream)));
@@ -171,9 +191,31 @@ qsa_status qsa_select_step(const float* q32, uint16_t* q16, const uint16_t* kb, 
   if (!aligned(q32, 16) || !aligned(q16, 16)) return QSA_ERR_MISALIGNED;
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  if (q16 && g.nb > 0 && use_separate(nq, H, *dev)) {
+    cudaStream_t s = as_cuda(stream);
+    const int64_t n = static_cast<int64_t>(nq) * H * D;
+    if ((st = from_cuda(qsa::launch_convert(q32, q16, n, *dev, s))) != QSA_OK) return st;
+    return run_separate(q16, kb, nq, H, D, g, k, scores, ids, *dev, s);
+  }
   qsa::FusedProblem p{q32, nullptr, q16, kb, scores, ids, nq, H, D, g.nb, g.n_full,
                       g.has_tail, k, 1, 0};
   return from_cuda(qsa::launch_fused(p, *dev, as_cuda(stream)));
+}
+
+int32_t qsa_select_step_launches(int32_t nq, int32_t H, int32_t D, int64_t n_kv, int32_t block,
+                                 int32_t k, int32_t with_q16) {
+  if (nq < 0 || n_kv < 0 || block < 1 || H < 1 || D < 1 || k < 1) return -1;
+  if (!supported_heads(H) || D % 16 != 0 || D < 16 || D > 256 || k > qsa::kMaxSelectK) return -1;
+  const int64_t nb = n_kv / block + (n_kv % block != 0 ? 1 : 0);
+  if (nb > qsa::kMaxSelectNb || static_cast<int64_t>(nq) * H > 0x7FFFFFFFLL) return -1;
+  if (nq == 0 || nb == 0) return 0;
+  const DeviceInfo* dev = nullptr;
+  if (device_or_error(&dev) != QSA_OK) return -1;
+  if (!with_q16 || !use_separate(nq, H, *dev)) return 1;
+  // convert (nq * H * D is a multiple of 8: one vector launch), the score
+  // kernel when there are full blocks, the tail kernel when there is a tail,
+  // and the select.
+  return 1 + (n_kv / block > 0 ? 1 : 0) + (n_kv % block != 0 ? 1 : 0) + 1;
 }
 
 // Shared by the two batched entry points: batch count and kb stride rules.

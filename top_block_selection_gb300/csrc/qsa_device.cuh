@@ -26,6 +26,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Let the next kernel on the stream begin its set-up now.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until every earlier kernel this one depends on has finished and its
+// memory is visible; call before the first read of their outputs.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

@@ -3,10 +3,30 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace qsa {
+
+// Launches `kernel` with programmatic stream serialization: it may start
+// while the previous kernel on the stream finishes; the kernel itself must
+// call pdl_wait() before reading what earlier work produced.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct DeviceInfo {
   int id = -1;
@@ -67,6 +87,8 @@ struct FusedProblem {
   int64_t kb_batch_stride;  // kb elements between batches; 0 = kb shared by all batches
 };
 cudaError_t init_fused_kernels(const DeviceInfo& dev);
+// CTAs the fused kernel would launch for one batch of nq queries of H heads.
+int64_t fused_blocks(int32_t nq, int32_t H, const DeviceInfo& dev);
 cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStream_t stream);
 
 cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k, int32_t* ids,

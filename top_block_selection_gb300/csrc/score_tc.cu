@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   const int m0 = blockIdx.x * kTileM;
   const int col0 = blockIdx.y * a.bn;
 
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int c = 0; c < a.n_chunks; ++c) mbar_init(&bars[c], 1);
     mbar_init(mma_bar, 1);
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_d = *tmem_slot;
+  pdl_wait();  // q and kb may come from the previous kernel on the stream
 
   if (threadIdx.x == 0) {
     const uint32_t chunk_bytes = static_cast<uint32_t>((kTileM + a.bn) * kRowBytes);
@@ -157,6 +159,8 @@ __global__ void __launch_bounds__(kTailThreads)
     tail_kernel(const __half* __restrict__ q, const __half* __restrict__ kb_tail,
                 float* __restrict__ scores, int32_t nq, int32_t H, int32_t D, int64_t nb) {
   __shared__ float acc_s[kTailThreads];
+  pdl_launch_dependents();
+  pdl_wait();
   const int q_per_block = kTailThreads / H;
   const int ql = threadIdx.x / H;
   const int h = threadIdx.x - ql * H;
@@ -287,25 +291,25 @@ cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStre
     if (smem > static_cast<size_t>(dev.max_smem_optin)) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(m_tiles), static_cast<unsigned>(n_tiles));
     const dim3 block(kScoreThreads);
+    cudaError_t e;
     switch (p.H) {
-      case 1: score_tc_kernel<1><<<grid, block, smem, stream>>>(tm_kb, tm_q, a); break;
-      case 2: score_tc_kernel<2><<<grid, block, smem, stream>>>(tm_kb, tm_q, a); break;
-      case 4: score_tc_kernel<4><<<grid, block, smem, stream>>>(tm_kb, tm_q, a); break;
-      case 8: score_tc_kernel<8><<<grid, block, smem, stream>>>(tm_kb, tm_q, a); break;
-      case 16: score_tc_kernel<16><<<grid, block, smem, stream>>>(tm_kb, tm_q, a); break;
-      case 32: score_tc_kernel<32><<<grid, block, smem, stream>>>(tm_kb, tm_q, a); break;
+      case 1: e = launch_pdl(score_tc_kernel<1>, grid, block, smem, stream, tm_kb, tm_q, a); break;
+      case 2: e = launch_pdl(score_tc_kernel<2>, grid, block, smem, stream, tm_kb, tm_q, a); break;
+      case 4: e = launch_pdl(score_tc_kernel<4>, grid, block, smem, stream, tm_kb, tm_q, a); break;
+      case 8: e = launch_pdl(score_tc_kernel<8>, grid, block, smem, stream, tm_kb, tm_q, a); break;
+      case 16: e = launch_pdl(score_tc_kernel<16>, grid, block, smem, stream, tm_kb, tm_q, a); break;
+      case 32: e = launch_pdl(score_tc_kernel<32>, grid, block, smem, stream, tm_kb, tm_q, a); break;
       default: return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (p.nq > 0 && p.has_tail) {
     const int q_per_block = kTailThreads / p.H;
     const int64_t grid = (p.nq + q_per_block - 1) / q_per_block;
-    tail_kernel<<<static_cast<unsigned>(grid), kTailThreads, 0, stream>>>(
-        reinterpret_cast<const __half*>(p.q),
-        reinterpret_cast<const __half*>(p.kb) + (p.nb - 1) * p.D, p.scores, p.nq, p.H, p.D, p.nb);
-    return cudaGetLastError();
+    return launch_pdl(tail_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTailThreads), 0, stream,
+                      reinterpret_cast<const __half*>(p.q),
+                      reinterpret_cast<const __half*>(p.kb) + (p.nb - 1) * p.D, p.scores, p.nq,
+                      p.H, p.D, p.nb);
   }
   return cudaSuccess;
 }

@@ -33,7 +33,9 @@ __global__ void __launch_bounds__(kSelThreads)
   const int g = threadIdx.x / T;
   const int gtid = threadIdx.x % T;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * groups + g;
+  pdl_launch_dependents();
   if (row >= nq) return;  // whole groups leave together; no CTA-wide barrier follows
+  pdl_wait();             // the scores may come from the previous kernel on the stream
   uint8_t* base = sm_raw + g * select_group_bytes(nb, k);
   uint32_t* hist = reinterpret_cast<uint32_t*>(base);                 // [kSelHistBins]
   uint64_t* cand = reinterpret_cast<uint64_t*>(hist + kSelHistBins);  // [kSelBinMax]
@@ -75,9 +77,8 @@ cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k
   while (groups > 1 && static_cast<size_t>(groups) * per > room) groups >>= 1;
   if (per > room) return cudaErrorInvalidValue;
   const int64_t grid = (static_cast<int64_t>(nq) + groups - 1) / groups;
-  select_kernel<<<static_cast<unsigned>(grid), groups * 32 * kSelG, groups * per, stream>>>(
-      scores, nq, nb, k, ids);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, dim3(static_cast<unsigned>(grid)), dim3(groups * 32 * kSelG),
+                    groups * per, stream, scores, nq, nb, k, ids);
 }
 
 }  // namespace qsa
