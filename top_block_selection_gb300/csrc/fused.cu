@@ -190,6 +190,33 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
     fence_mbarrier_init();
     if (n_local > 0) tma_prefetch_desc(&tm_kb);
     if (!kF32Q && need_q) tma_prefetch_desc(&tm_q);
+    // Start this CTA's first operand tiles on their way from HBM to L2 while
+    // the previous kernel finishes; the loads proper come after the wait.
+    for (int t = 0; t < 2 && t < n_local; ++t)
+      for (int c = 0; c < a.n_chunks; ++c)
+        tma_prefetch_l2_3d(&tm_kb, c * kFKAtom, (rank + t * kCluster) * kFTileM, kb_z);
+    if (need_q) {
+      if (kF32Q) {
+        const char* qp = reinterpret_cast<const char*>(q32b + static_cast<int64_t>(col0) * a.D);
+        const uint32_t q_bytes = static_cast<uint32_t>(qh_rows) * a.D * 4u;
+        for (uint32_t off = 0; off < q_bytes; off += 16384u)
+          bulk_prefetch_l2(qp + off, min(16384u, q_bytes - off));
+      } else {
+        for (int c = 0; c < a.n_chunks; ++c)
+          tma_prefetch_l2_2d(&tm_q, c * kFKAtom, q_row0 + col0);
+      }
+    }
+  }
+  // The TMEM allocation comes before the wait too, and every CTA then gives
+  // up its allocation permit, also one that allocates nothing: a CTA holding
+  // the permit keeps the SM from taking another CTA (measured: ranks without
+  // tiles that kept it halved the resident clusters, and early-launched CTAs
+  // that kept it across the wait held back half the next step's clusters
+  // until the previous step had completed).
+  if (producer_warp) {
+    __syncwarp();
+    if (n_local > 0) tmem_alloc(&tmem_slot, a.tmem_cols);
+    tmem_relinquish();
   }
   pdl_wait();
   if (tid == kProducerWarp * 32) {
@@ -210,14 +237,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
   // CTA of the cluster has started (this arrive, the wait below).
   if (a.dsmem) cluster_arrive_release();
   __syncwarp();
-  if (producer_warp) {
-    if (n_local > 0) tmem_alloc(&tmem_slot, a.tmem_cols);
-    // Every CTA gives up its TMEM allocation permit, also one that allocates
-    // nothing: a CTA still holding the permit kept the SM from taking
-    // another CTA (measured: ranks without tiles halved the resident
-    // clusters).
-    tmem_relinquish();
-  } else if (kF32Q && need_q) {
+  if (!producer_warp && kF32Q && need_q) {
     // fp32 queries -> fp16 (round to nearest even) -> swizzled operand tile,
     // by the kWork threads. Rows past the last query and columns past D are 0.
     const int f4_per_row = a.n_chunks * (kFKAtom / 4);
