@@ -438,14 +438,20 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
     const uint32_t* rk = reinterpret_cast<const uint32_t*>(smem + a.rows_off + r * a.row_bytes);
     if (a.nb <= 8 * kWork) {
       uint32_t key[8];
-      if (a.dsmem) load_keys_smem<kWork, 8>(rk, a.nb, key, hist, tid, 1);
-      else load_keys_global<kWork, 8>(row, a.nb, key, hist, tid, 1);
-      select_row_regs<kWork, 8>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1);
+      if (a.dsmem) load_keys_regs<kWork, 8>(rk, a.nb, key, hist, tid);
+      else load_keys_regs_global<kWork, 8>(row, a.nb, key, hist, tid);
+      if (!select_row_window<kWork, 8>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1)) {
+        build_first_digit_hist<kWork, 8>(key, a.nb, hist, tid, 1);
+        select_row_regs<kWork, 8>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1);
+      }
     } else if (a.nb <= 16 * kWork) {
       uint32_t key[16];
-      if (a.dsmem) load_keys_smem<kWork, 16>(rk, a.nb, key, hist, tid, 1);
-      else load_keys_global<kWork, 16>(row, a.nb, key, hist, tid, 1);
-      select_row_regs<kWork, 16>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1);
+      if (a.dsmem) load_keys_regs<kWork, 16>(rk, a.nb, key, hist, tid);
+      else load_keys_regs_global<kWork, 16>(row, a.nb, key, hist, tid);
+      if (!select_row_window<kWork, 16>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1)) {
+        build_first_digit_hist<kWork, 16>(key, a.nb, hist, tid, 1);
+        select_row_regs<kWork, 16>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1);
+      }
     } else {
       const uint32_t* keys = rk;
       if (!a.dsmem) {

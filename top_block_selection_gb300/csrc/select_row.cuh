@@ -7,10 +7,12 @@
 // -0.0 == +0.0; ids past nb are -1.
 //
 // Scores are compared as order-preserving uint32 keys (score_key). The search
-// is a radix select on the keys, most significant digit first:
+// is a radix select on the keys, most significant digit first. Register-held
+// rows try a first digit measured down from the row's largest key
+// (select_row_window), which nearly always settles the search in one pass;
+// otherwise, and for rows in shared memory:
 //   * the first digit is fixed, the top 11 key bits (sign, exponent, two
-//     mantissa bits: quarter-octave bins), so its histogram can be built
-//     while the row is loaded, or by whoever produces the scores;
+//     mantissa bits: quarter-octave bins);
 //   * one suffix scan over the bins finds the digit holding the k-th largest
 //     key; every key in a higher bin is a winner;
 //   * the search stops as soon as (a) the keys still needed fill the boundary
@@ -35,6 +37,8 @@ constexpr int kSelFirstBits = 11;
 constexpr int kSelFirstShift = 32 - kSelFirstBits;
 constexpr int kSelHistBins = 1 << kSelFirstBits;
 constexpr int kSelCandMax = 32;
+constexpr int kSelBinMax = 256;
+constexpr int kSelRankMax = 32;
 
 struct SelectShared {
   uint32_t wsum[32];
@@ -166,202 +170,13 @@ __device__ __forceinline__ void scan_bins(const uint32_t* hist, int nbins, uint3
   else scan_bins_fixed<T, 256>(hist, need, sh, gtid, bar_id);
 }
 
-// Top-k of one row, keys staged in shared memory (any nb up to the shared
-// memory budget). With kFromGlobal the row is read from `s` (ld.global.cg:
-// it may have been written by other CTAs of the same kernel) into keys[] and
-// the first-digit histogram is built here; otherwise keys[0..nb) and the
-// first-digit histogram in hist[] must already be complete.
-// Shared arrays of this group: keys[nb], hist[kSelHistBins] (16-byte
-// aligned), cand[kSelCandMax], sel[min(k, nb)].
-template <int T, bool kFromGlobal>
-__device__ void select_row_smem(const float* s, int nb, int k, int32_t* __restrict__ out,
-                           uint32_t* keys, uint32_t* hist, uint64_t* cand, uint64_t* sel,
-                           SelectShared& sh, int gtid, int bar_id) {
-  const int kk = k < nb ? k : nb;
-
-  if (kFromGlobal) {
-    for (int i = gtid; i < kSelHistBins; i += T) hist[i] = 0;
-    group_sync<T>(bar_id);
-    for (int base = 0; base < nb; base += 8 * T) {
-      float v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = base + j * T + gtid;
-        v[j] = i < nb ? __ldcg(s + i) : 0.0f;
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = base + j * T + gtid;
-        if (i < nb) {
-          const uint32_t key = score_key(v[j]);
-          keys[i] = key;
-          atomicAdd(&hist[key >> kSelFirstShift], 1u);
-        }
-      }
-    }
-    group_sync<T>(bar_id);
-  }
-
-  enum Mode { kTakeAll, kTies, kCand };
-  Mode mode = kTakeAll;
-  uint32_t thr = 0;  // kTakeAll: key >= thr; kTies: key > thr, then ties by index
-  uint32_t need = static_cast<uint32_t>(kk);
-  uint32_t prefix = 0;  // kCand: candidates share the key bits [hi, 32) with prefix
-  int hi = 32;
-  if (kk > 0 && kk < nb) {
-    int nbits = kSelFirstBits;
-    bool first = true;
-    while (true) {
-      const int lo = hi - nbits;
-      const int nbins = 1 << nbits;
-      if (!first) {
-        const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
-        for (int i = gtid; i < 256; i += T) hist[i] = 0;  // refinement scans read 256 bins
-        group_sync<T>(bar_id);
-        for (int i = gtid; i < nb; i += T) {
-          const uint32_t key = keys[i];
-          if (((key ^ prefix) >> hi) == 0) atomicAdd(&hist[(key >> lo) & dmask], 1u);
-        }
-        group_sync<T>(bar_id);
-      }
-      first = false;
-      scan_bins<T>(hist, nbins, need, sh, gtid, bar_id);
-      const uint32_t digit = sh.digit, above = sh.above, cnt = sh.cnt;
-      need -= above;
-      prefix |= digit << lo;
-      hi = lo;
-      if (cnt == need) {
-        mode = kTakeAll;
-        thr = prefix;
-        break;
-      }
-      if (hi == 0) {
-        mode = kTies;
-        thr = prefix;
-        break;
-      }
-      if (cnt <= static_cast<uint32_t>(kSelCandMax)) {
-        mode = kCand;
-        break;
-      }
-      nbits = hi < 8 ? hi : 8;
-      group_sync<T>(bar_id);  // every thread has read sh before the next pass
-    }
-  }
-
-  if (kk > 0) {
-    // Gather: count, scan, write. Winners go to sel[0, n_win), candidates to
-    // cand[0, n_cand).
-    const uint32_t bin_top = (mode == kCand) ? (prefix | ((1u << hi) - 1u)) : 0u;
-    uint32_t n_w = 0, n_c = 0;
-    for (int i = gtid; i < nb; i += T) {
-      const uint32_t key = keys[i];
-      if (mode == kTakeAll) {
-        n_w += key >= thr ? 1u : 0u;
-      } else if (mode == kTies) {
-        n_w += key > thr ? 1u : 0u;
-      } else {
-        const bool w = key > bin_top;
-        n_w += w ? 1u : 0u;
-        n_c += (!w && ((key ^ prefix) >> hi) == 0) ? 1u : 0u;
-      }
-    }
-    uint32_t totals;
-    const uint32_t offs = group_excl_scan<T>((n_w << 16) | n_c, &totals, sh, gtid, bar_id);
-    uint32_t wo = offs >> 16, co = offs & 0xFFFFu;
-    const uint32_t n_win = totals >> 16, n_cand = totals & 0xFFFFu;
-    for (int i = gtid; i < nb; i += T) {
-      const uint32_t key = keys[i];
-      bool w, c = false;
-      if (mode == kTakeAll) {
-        w = key >= thr;
-      } else if (mode == kTies) {
-        w = key > thr;
-      } else {
-        w = key > bin_top;
-        c = !w && ((key ^ prefix) >> hi) == 0;
-      }
-      if (w) sel[wo++] = win_key(key, i);
-      if (c) cand[co++] = win_key(key, i);
-    }
-    group_sync<T>(bar_id);
-    if (mode == kCand) {
-      // The boundary bin's `need` largest candidates complete the winners.
-      const uint32_t nd = need;
-      split_rank<T>(cand, static_cast<int>(n_cand), gtid, [&](int e, uint32_t r) {
-        if (r < nd) sel[n_win + r] = cand[e];
-      });
-      group_sync<T>(bar_id);
-    } else if (mode == kTies) {
-      // Keys equal to thr, in index order, until `need` are taken.
-      uint32_t taken = 0;  // uniform over the group
-      for (int base = 0; base < nb && taken < need; base += T) {
-        const int i = base + gtid;
-        const bool tie = i < nb && keys[i] == thr;
-        uint32_t tot;
-        const uint32_t r = taken + group_excl_scan<T>(tie ? 1u : 0u, &tot, sh, gtid, bar_id);
-        if (tie && r < need) sel[n_win + r] = win_key(thr, i);
-        taken += tot;
-      }
-      group_sync<T>(bar_id);
-    }
-  }
-
-  // Output slot of every winner = its rank among the winners.
-  split_rank<T>(sel, kk, gtid, [&](int e, uint32_t r) {
-    out[r] = static_cast<int32_t>(~static_cast<uint32_t>(sel[e]));
-  });
-  for (int j = kk + gtid; j < k; j += T) out[j] = -1;
-}
-
 // ------------------------------------------------- register-resident keys
 // Thread gtid holds the keys of indices j*T + gtid, j < R (key 0 past nb: it
 // is below every finite score's key). Fewer instructions per element than
 // the shared-memory path, for rows with nb <= R*T.
 
-// Loads a row of scores (ld.global.cg) into registers and builds the
-// first-digit histogram (hist[kSelHistBins] in shared memory).
-template <int T, int R>
-__device__ __forceinline__ void load_keys_global(const float* s, int nb, uint32_t (&key)[R],
-                                                 uint32_t* hist, int gtid, int bar_id) {
-  for (int i = gtid; i < kSelHistBins; i += T) hist[i] = 0;
-  float v[R];
-#pragma unroll
-  for (int j = 0; j < R; ++j) {
-    const int i = j * T + gtid;
-    v[j] = i < nb ? __ldcg(s + i) : 0.0f;
-  }
-  group_sync<T>(bar_id);
-#pragma unroll
-  for (int j = 0; j < R; ++j) {
-    const int i = j * T + gtid;
-    key[j] = i < nb ? score_key(v[j]) : 0u;
-    if (i < nb) atomicAdd(&hist[key[j] >> kSelFirstShift], 1u);
-  }
-  group_sync<T>(bar_id);
-}
-
-// Loads keys already in shared memory (keys[nb]) into registers and builds
-// the first-digit histogram.
-template <int T, int R>
-__device__ __forceinline__ void load_keys_smem(const uint32_t* keys, int nb, uint32_t (&key)[R],
-                                               uint32_t* hist, int gtid, int bar_id) {
-  for (int i = gtid; i < kSelHistBins; i += T) hist[i] = 0;
-#pragma unroll
-  for (int j = 0; j < R; ++j) {
-    const int i = j * T + gtid;
-    key[j] = i < nb ? keys[i] : 0u;
-  }
-  group_sync<T>(bar_id);
-#pragma unroll
-  for (int j = 0; j < R; ++j) {
-    if (j * T + gtid < nb) atomicAdd(&hist[key[j] >> kSelFirstShift], 1u);
-  }
-  group_sync<T>(bar_id);
-}
-
 // Top-k of one row whose keys are in registers and whose first-digit
-// histogram is complete in hist (see the loaders above).
+// histogram is complete in hist (build_first_digit_hist below).
 template <int T, int R>
 __device__ void select_row_regs(const uint32_t (&key)[R], int nb, int k, int32_t* __restrict__ out,
                                 uint32_t* hist, uint64_t* cand, uint64_t* sel, SelectShared& sh,
@@ -477,6 +292,141 @@ __device__ void select_row_regs(const uint32_t (&key)[R], int nb, int k, int32_t
   for (int j = kk + gtid; j < k; j += T) out[j] = -1;
 }
 
+// ------------------------------------------------ window select (registers)
+// The same search with a first digit measured down from the row's largest
+// key M: digit kSelHistBins-1-b holds the keys with (M - key) >> kSelWinShift
+// == b, for b < kSelHistBins - 1 (the 32 octaves of fp32 below M in steps of
+// 1/64 octave, wide enough to reach past a +1e9 tail score); keys further
+// below get digit 0 and are not counted. Score
+// rows are dense near their top, so the k-th largest key nearly always lies
+// in the window, in a bin of a few keys: one histogram and one scan finish
+// the search, and the boundary bin's keys are ranked directly. Otherwise
+// (the k-th key below the window, or more than kSelBinMax keys in its bin)
+// the function returns false having written only hist and sh, and the
+// caller runs the fixed-digit select (select_row_regs). hist must be zero on
+// entry; keys past nb are 0.
+constexpr int kSelWinShift = 17;
+
+// Loads keys already in shared memory into registers and zeroes hist (the
+// first barrier of select_row_window orders the zeroing).
+template <int T, int R>
+__device__ __forceinline__ void load_keys_regs(const uint32_t* keys, int nb, uint32_t (&key)[R],
+                                               uint32_t* hist, int gtid) {
+  for (int i = gtid * 4; i < kSelHistBins; i += T * 4)
+    *reinterpret_cast<uint4*>(hist + i) = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    const int i = j * T + gtid;
+    key[j] = i < nb ? keys[i] : 0u;
+  }
+}
+
+// The same from a row of scores in global memory (ld.global.cg).
+template <int T, int R>
+__device__ __forceinline__ void load_keys_regs_global(const float* s, int nb, uint32_t (&key)[R],
+                                                      uint32_t* hist, int gtid) {
+  float v[R];
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    const int i = j * T + gtid;
+    v[j] = i < nb ? __ldcg(s + i) : 0.0f;
+  }
+  for (int i = gtid * 4; i < kSelHistBins; i += T * 4)
+    *reinterpret_cast<uint4*>(hist + i) = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int j = 0; j < R; ++j) key[j] = j * T + gtid < nb ? score_key(v[j]) : 0u;
+}
+
+// Rebuilds hist as the fixed first-digit histogram of register keys (the
+// entry state of select_row_regs).
+template <int T, int R>
+__device__ __forceinline__ void build_first_digit_hist(const uint32_t (&key)[R], int nb,
+                                                       uint32_t* hist, int gtid, int bar_id) {
+  for (int i = gtid * 4; i < kSelHistBins; i += T * 4)
+    *reinterpret_cast<uint4*>(hist + i) = make_uint4(0u, 0u, 0u, 0u);
+  group_sync<T>(bar_id);
+#pragma unroll
+  for (int j = 0; j < R; ++j)
+    if (j * T + gtid < nb) atomicAdd(&hist[key[j] >> kSelFirstShift], 1u);
+  group_sync<T>(bar_id);
+}
+
+template <int T, int R>
+__device__ bool select_row_window(const uint32_t (&key)[R], int nb, int k,
+                                  int32_t* __restrict__ out, uint32_t* hist, uint64_t* cand,
+                                  uint64_t* sel, SelectShared& sh, int gtid, int bar_id) {
+  constexpr int kWarps = T / 32;
+  constexpr uint32_t kTop = kSelHistBins - 1;
+  const int kk = k < nb ? k : nb;
+  uint32_t M = 0;
+  uint32_t bdig = 0;                      // the boundary digit
+  uint32_t need = static_cast<uint32_t>(kk);  // keys still needed from its bin
+  bool take_bin = true;                   // the boundary bin is taken whole
+  if (kk > 0 && kk < nb) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < R; ++j) m = max(m, key[j]);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((gtid & 31) == 0) sh.wsum[gtid >> 5] = m;
+    if (gtid == 0) sh.cnt = 0xFFFFFFFFu;  // stays so unless the scan finds the digit
+    group_sync<T>(bar_id);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = max(M, sh.wsum[w]);
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const uint32_t t = (M - key[j]) >> kSelWinShift;
+      if (j * T + gtid < nb && t < kTop) atomicAdd(&hist[kTop - t], 1u);
+    }
+    group_sync<T>(bar_id);
+    scan_bins_fixed<T, kSelHistBins>(hist, need, sh, gtid, bar_id);
+    const uint32_t cnt = sh.cnt;
+    if (cnt == 0xFFFFFFFFu) return false;  // the k-th key lies below the window
+    bdig = sh.digit;
+    need -= sh.above;
+    take_bin = cnt == need;
+    if (!take_bin && cnt > static_cast<uint32_t>(kSelBinMax)) return false;
+  }
+
+  if (kk > 0) {
+    uint32_t wmask = 0, cmask = 0;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const bool valid = j * T + gtid < nb;
+      const uint32_t t = (M - key[j]) >> kSelWinShift;
+      const uint32_t d = t < kTop ? kTop - t : 0u;
+      const bool w = valid && (kk == nb || d > bdig || (take_bin && d == bdig));
+      const bool c = valid && !take_bin && d == bdig;
+      wmask |= (w ? 1u : 0u) << j;
+      cmask |= (c ? 1u : 0u) << j;
+    }
+    uint32_t totals;
+    const uint32_t offs = group_excl_scan<T>((static_cast<uint32_t>(__popc(wmask)) << 16) |
+                                                 static_cast<uint32_t>(__popc(cmask)),
+                                             &totals, sh, gtid, bar_id);
+    uint32_t wo = offs >> 16, co = offs & 0xFFFFu;
+    const uint32_t n_win = totals >> 16, n_cand = totals & 0xFFFFu;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      if (wmask & (1u << j)) sel[wo++] = win_key(key[j], j * T + gtid);
+      if (cmask & (1u << j)) cand[co++] = win_key(key[j], j * T + gtid);
+    }
+    group_sync<T>(bar_id);
+    if (!take_bin) {
+      const uint32_t nd = need;
+      split_rank<T>(cand, static_cast<int>(n_cand), gtid, [&](int e, uint32_t r) {
+        if (r < nd) sel[n_win + r] = cand[e];
+      });
+      group_sync<T>(bar_id);
+    }
+  }
+
+  split_rank<T>(sel, kk, gtid, [&](int e, uint32_t r) {
+    out[r] = static_cast<int32_t>(~static_cast<uint32_t>(sel[e]));
+  });
+  for (int j = kk + gtid; j < k; j += T) out[j] = -1;
+  return true;
+}
+
 // ------------------------------------------------ G-warp select, keys in smem
 // A group of G warps (T = 32 G threads) selects one row whose keys are in
 // shared memory. Per-element work is a histogram increment and two compares;
@@ -485,8 +435,6 @@ __device__ void select_row_regs(const uint32_t (&key)[R], int nb, int k, int32_t
 // kSelBinMax of them) are compacted and only they are refined, 8 bits at a
 // time, until the keys still needed fill a bin or at most kSelRankMax remain,
 // which are ranked pairwise.
-constexpr int kSelBinMax = 256;
-constexpr int kSelRankMax = 32;
 
 struct GroupShared {
   uint32_t wsum[8];
