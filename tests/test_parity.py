@@ -98,7 +98,7 @@ def test_ragged_tiles(tbs, nq, nb, tail):
     check_case(tbs, q, kb, n_kv, block, 8, f"ragged-{nq}-{nb}-{tail}")
 
 
-@pytest.mark.parametrize("H,D", [(1, 64), (2, 256), (4, 48), (16, 128), (32, 32)])
+@pytest.mark.parametrize("H,D", [(1, 64), (2, 256), (4, 48), (16, 128), (32, 32), (8, 192), (4, 160)])
 def test_other_geometries(tbs, H, D):
     nq, nb = 45, 700
     q, kb = qi.random_case(nq, H, D, nb, seed=H * 7 + D, scale=0.5)

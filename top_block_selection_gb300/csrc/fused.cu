@@ -241,32 +241,65 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
     // fp32 queries -> fp16 (round to nearest even) -> swizzled operand tile,
     // by the kWork threads. Rows past the last query and columns past D are 0.
     const int f4_per_row = a.n_chunks * (kFKAtom / 4);
-    const int total = a.bn * f4_per_row;
-    for (int base = 0; base < total; base += 8 * kWork) {
-      float4 v[8];
+    if (kWork % f4_per_row == 0) {
+      // Each thread keeps one 4-column group and steps down the rows.
+      const int rstep = kWork / f4_per_row;
+      const int i = (tid % f4_per_row) * 4;
+      const int r0 = tid / f4_per_row;
+      const bool col_ok = i < a.D;
+      const int64_t src_step = static_cast<int64_t>(rstep) * a.D;
+      const float* src = q32b + static_cast<int64_t>(col0 + r0) * a.D + i;
+      for (int base = r0; base < a.bn; base += 8 * rstep, src += 8 * src_step) {
+        float4 v[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int f = base + j * kWork + tid;
-        const int row = f / f4_per_row;
-        const int i = (f - row * f4_per_row) * 4;
-        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (f < total && row < qh_rows && i < a.D)
-          v[j] = __ldg(reinterpret_cast<const float4*>(q32b + static_cast<int64_t>(col0 + row) * a.D + i));
+        for (int j = 0; j < 8; ++j) {
+          v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (base + j * rstep < qh_rows && col_ok)
+            v[j] = __ldg(reinterpret_cast<const float4*>(src + j * src_step));
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int row = base + j * rstep;
+          if (row < a.bn) {
+            const __half2 h01 = __floats2half2_rn(v[j].x, v[j].y);
+            const __half2 h23 = __floats2half2_rn(v[j].z, v[j].w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<const uint32_t*>(&h01);
+            pk.y = *reinterpret_cast<const uint32_t*>(&h23);
+            *reinterpret_cast<uint2*>(sQ + sw128_offset(a.bn, row, i)) = pk;
+            if (q16outb != nullptr && rank == 0 && row < qh_rows && col_ok)
+              *reinterpret_cast<uint2*>(q16outb + static_cast<int64_t>(col0 + row) * a.D + i) = pk;
+          }
+        }
       }
+    } else {
+      const int total = a.bn * f4_per_row;
+      for (int base = 0; base < total; base += 8 * kWork) {
+        float4 v[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int f = base + j * kWork + tid;
-        if (f < total) {
+        for (int j = 0; j < 8; ++j) {
+          const int f = base + j * kWork + tid;
           const int row = f / f4_per_row;
           const int i = (f - row * f4_per_row) * 4;
-          const __half2 h01 = __floats2half2_rn(v[j].x, v[j].y);
-          const __half2 h23 = __floats2half2_rn(v[j].z, v[j].w);
-          uint2 pk;
-          pk.x = *reinterpret_cast<const uint32_t*>(&h01);
-          pk.y = *reinterpret_cast<const uint32_t*>(&h23);
-          *reinterpret_cast<uint2*>(sQ + sw128_offset(a.bn, row, i)) = pk;
-          if (q16outb != nullptr && rank == 0 && row < qh_rows && i < a.D)
-            *reinterpret_cast<uint2*>(q16outb + static_cast<int64_t>(col0 + row) * a.D + i) = pk;
+          v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (f < total && row < qh_rows && i < a.D)
+            v[j] = __ldg(reinterpret_cast<const float4*>(q32b + static_cast<int64_t>(col0 + row) * a.D + i));
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int f = base + j * kWork + tid;
+          if (f < total) {
+            const int row = f / f4_per_row;
+            const int i = (f - row * f4_per_row) * 4;
+            const __half2 h01 = __floats2half2_rn(v[j].x, v[j].y);
+            const __half2 h23 = __floats2half2_rn(v[j].z, v[j].w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<const uint32_t*>(&h01);
+            pk.y = *reinterpret_cast<const uint32_t*>(&h23);
+            *reinterpret_cast<uint2*>(sQ + sw128_offset(a.bn, row, i)) = pk;
+            if (q16outb != nullptr && rank == 0 && row < qh_rows && i < a.D)
+              *reinterpret_cast<uint2*>(q16outb + static_cast<int64_t>(col0 + row) * a.D + i) = pk;
+          }
         }
       }
     }
