@@ -100,18 +100,27 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
-__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+// Remote store that signals its 4 bytes on the destination CTA's mbarrier
+// (both addresses in the same peer CTA).
+__device__ __forceinline__ void st_async_u32(uint32_t addr, uint32_t v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(
+                   addr),
+               "r"(v), "r"(bar)
+               : "memory");
 }
 
 // Sends one score's key to keys[b] of the row's region in the CTA that
-// selects the row (rank ql % 8, row slot ql / 8). A plain remote store: the
-// owner builds the row's histogram itself, since remote atomics are slow.
-__device__ __forceinline__ void send_key(uint32_t rows_base, uint32_t row_bytes, int ql, int b,
-                                         float score) {
+// selects the row (rank ql % 8, row slot ql / 8), counted on that CTA's
+// bar_keys. A remote store, not a remote atomic (those are slow): the owner
+// builds the row's histogram itself. The owner waits on its own barrier for
+// the bytes of all its rows, so no cluster-wide release (which would also
+// wait for this thread's global score stores) is needed.
+__device__ __forceinline__ void send_key(uint32_t rows_base, uint32_t row_bytes, uint32_t bar_keys,
+                                         int ql, int b, float score) {
+  const uint32_t owner = static_cast<uint32_t>(ql & 7);
   const uint32_t local = rows_base + static_cast<uint32_t>(ql >> 3) * row_bytes;
-  const uint32_t remote = cluster_map(local, static_cast<uint32_t>(ql & 7));
-  st_cluster_u32(remote + static_cast<uint32_t>(b) * 4u, score_key(score));
+  st_async_u32(cluster_map(local, owner) + static_cast<uint32_t>(b) * 4u, score_key(score),
+               cluster_map(bar_keys, owner));
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -138,7 +147,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
                       const __grid_constant__ CUtensorMap tm_q, const FusedArgs a) {
   static_assert(32 % H == 0, "a 32-column TMEM load must hold whole queries");
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_full[2], bar_empty[2], bar_acc_full[2], bar_acc_empty[2], bar_q;
+  __shared__ uint64_t bar_full[2], bar_empty[2], bar_acc_full[2], bar_acc_empty[2], bar_q, bar_keys;
   __shared__ uint32_t tmem_slot;
   __shared__ int failed;
   __shared__ float tail_acc[256];
@@ -172,6 +181,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
   const bool need_q = n_local > 0 || tail_owner || (kF32Q && q16outb != nullptr && rank == 0);
   const int rows_here = a.qg > rank ? (a.qg - rank + kCluster - 1) / kCluster : 0;
   const uint32_t rows_base = smem_u32(smem + a.rows_off);
+  const uint32_t keys_bar = smem_u32(&bar_keys);
   const bool producer_warp = warp == kProducerWarp;
 
   // Programmatic dependent launch: the next kernel on the stream may start its
@@ -186,8 +196,16 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
       mbar_init(&bar_acc_empty[s], kWork);
     }
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_keys, 1);
     failed = 0;
     fence_mbarrier_init();
+    // DSMEM mode: this CTA expects the keys of its valid rows (nb keys each),
+    // registered before the cluster barrier that lets peers send.
+    if (a.dsmem) {
+      int rows_valid = 0;
+      for (int r = 0; r < rows_here && q0 + rank + r * kCluster < a.nq; ++r) ++rows_valid;
+      mbar_arrive_expect_tx(&bar_keys, static_cast<uint32_t>(rows_valid * a.nb) * 4u);
+    }
     if (n_local > 0) tma_prefetch_desc(&tm_kb);
     if (!kF32Q && need_q) tma_prefetch_desc(&tm_q);
     // Start this CTA's first operand tiles on their way from HBM to L2 while
@@ -395,7 +413,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
         for (int h = 0; h < H; ++h) s = __fadd_rn(s, fmaxf(tail_acc[ql * H + h], 0.0f));
         const float score = __fadd_rn(s, 1.0e9f);
         scoresb[static_cast<int64_t>(q0 + ql) * a.nb + (a.nb - 1)] = score;
-        if (a.dsmem) send_key(rows_base, a.row_bytes, ql, a.nb - 1, score);
+        if (a.dsmem) send_key(rows_base, a.row_bytes, keys_bar, ql, a.nb - 1, score);
       }
     }
     // ---------------------------------------- epilogue (warps 0..7)
@@ -436,7 +454,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
           const int ql = c0 / H + j;
           if (b_ok && q0 + ql < a.nq) {
             out[static_cast<int64_t>(q0 + ql) * a.nb] = sc;
-            if (a.dsmem) send_key(rows_base, a.row_bytes, ql, b, sc);
+            if (a.dsmem) send_key(rows_base, a.row_bytes, keys_bar, ql, b, sc);
           }
         }
       }
@@ -450,10 +468,17 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
   __syncthreads();
   if (n_local > 0 && producer_warp) tmem_dealloc(tmem_base, a.tmem_cols);
 
-  // Every score (and, in DSMEM mode, every key) of the group is written and
-  // visible after this barrier.
-  cluster_sync_release_acquire();
-  if (producer_warp) return;  // the select runs on the kWork threads
+  if (a.dsmem) {
+    // Every key of this CTA's rows has arrived once bar_keys completes.
+    if (producer_warp) return;  // the select runs on the kWork threads
+    if (!mbar_wait_bounded(&bar_keys, 0, a.timeout_ns)) {
+      if (tid == 0) atomicOr(a.status, kErrFusedWaitTimeout);
+    }
+  } else {
+    // Every score of the group is written and visible after this barrier.
+    cluster_sync_release_acquire();
+    if (producer_warp) return;  // the select runs on the kWork threads
+  }
 
   // ---------------------------------------------------------- select
   // One row at a time with the kWork threads (the lowest latency per row).
