@@ -85,8 +85,11 @@ __device__ __forceinline__ void cluster_sync_release_acquire() {
           : "memory");
 }
 
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+// Arrive without release semantics: orders nothing but the CTA's start and
+// the mbarrier initialisation made visible by fence.mbarrier_init (a release
+// arrive waited about a microsecond here).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_wait_acquire() {
@@ -225,6 +228,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
       }
     }
   }
+  // DSMEM mode: peers store into this CTA's shared memory (keys, counted on
+  // bar_keys) only after every CTA of the cluster has started and initialised
+  // its barriers: this arrive, and the wait before a thread's first remote
+  // store. Arriving before the dependency wait lets the barrier complete
+  // while the previous kernel finishes.
+  __syncwarp();
+  if (a.dsmem) cluster_arrive_relaxed();
   // The TMEM allocation comes before the wait too, and every CTA then gives
   // up its allocation permit, also one that allocates nothing: a CTA holding
   // the permit keeps the SM from taking another CTA (measured: ranks without
@@ -251,9 +261,6 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
                     m * kFTileM, kb_z, &bar_full[t]);
     }
   }
-  // DSMEM mode: peers store into this CTA's shared memory only after every
-  // CTA of the cluster has started (this arrive, the wait below).
-  if (a.dsmem) cluster_arrive_release();
   __syncwarp();
   if (!producer_warp && kF32Q && need_q) {
     // fp32 queries -> fp16 (round to nearest even) -> swizzled operand tile,
