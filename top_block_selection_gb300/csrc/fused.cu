@@ -492,9 +492,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
   // Keys come from the row regions (DSMEM mode) or from global memory;
   // hist / cand / sel reuse the dead operand tiles.
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem);
-  uint64_t* cand = reinterpret_cast<uint64_t*>(hist + kSelHistBins);
+  uint32_t* excl = hist + kSelHistBins;
+  uint64_t* cand = reinterpret_cast<uint64_t*>(excl + kSelHistBins);
   uint64_t* sel = cand + kSelBinMax;
-  uint32_t* staged = reinterpret_cast<uint32_t*>(sel + a.k);
+  uint32_t* sel_bin = reinterpret_cast<uint32_t*>(sel + a.k);
+  uint32_t* staged = sel_bin + ((a.k + 3) & ~3);
   for (int r = 0; r < rows_here; ++r) {
     const int qi = q0 + rank + r * kCluster;
     if (qi >= a.nq) break;
@@ -505,7 +507,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
       uint32_t key[8];
       if (a.dsmem) load_keys_regs<kWork, 8>(rk, a.nb, key, hist, tid);
       else load_keys_regs_global<kWork, 8>(row, a.nb, key, hist, tid);
-      if (!select_row_window<kWork, 8>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1)) {
+      if (!select_row_window<kWork, 8>(key, a.nb, a.k, out, hist, excl, cand, sel, sel_bin, sel_sh,
+                                     tid, 1)) {
         build_first_digit_hist<kWork, 8>(key, a.nb, hist, tid, 1);
         select_row_regs<kWork, 8>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1);
       }
@@ -513,7 +516,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
       uint32_t key[16];
       if (a.dsmem) load_keys_regs<kWork, 16>(rk, a.nb, key, hist, tid);
       else load_keys_regs_global<kWork, 16>(row, a.nb, key, hist, tid);
-      if (!select_row_window<kWork, 16>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1)) {
+      if (!select_row_window<kWork, 16>(key, a.nb, a.k, out, hist, excl, cand, sel, sel_bin, sel_sh,
+                                      tid, 1)) {
         build_first_digit_hist<kWork, 16>(key, a.nb, hist, tid, 1);
         select_row_regs<kWork, 16>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1);
       }
@@ -662,10 +666,13 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
   const int rows_per_cta = (qg + kCluster - 1) / kCluster;
   const size_t operand_bytes = static_cast<size_t>(a.n_chunks) * (bn + 2 * kFTileM) * kFRowBytes;
   const size_t budget = static_cast<size_t>(dev.max_smem_optin) - g_fused_static_smem - 1024;
-  // Select scratch in the operand region after the epilogue: hist, cand, sel,
-  // and (global mode, long rows) the row's staged keys.
-  const size_t core = kSelHistBins * sizeof(uint32_t) +
-                      (static_cast<size_t>(kSelBinMax) + p.k) * sizeof(uint64_t);
+  // Select scratch in the operand region after the epilogue: hist, excl,
+  // cand, sel, sel_bin, and (global mode, long rows) the row's staged keys
+  // (16-byte aligned: k is rounded up to a multiple of 4).
+  const size_t k4 = (static_cast<size_t>(p.k) + 3) & ~static_cast<size_t>(3);
+  const size_t core = 2 * kSelHistBins * sizeof(uint32_t) +
+                      (static_cast<size_t>(kSelBinMax) + p.k) * sizeof(uint64_t) +
+                      k4 * sizeof(uint32_t);
   // DSMEM mode when the keys of the rows this CTA selects fit beside the
   // operand tiles.
   const size_t row_bytes = (static_cast<size_t>(a.nb) * sizeof(uint32_t) + 15) & ~static_cast<size_t>(15);

@@ -43,6 +43,7 @@ constexpr int kSelRankMax = 32;
 struct SelectShared {
   uint32_t wsum[32];
   uint32_t digit, above, cnt;
+  uint32_t n_cand;  // window select: candidates gathered so far
 };
 
 __device__ __forceinline__ uint32_t lane_mask_lt() {
@@ -159,6 +160,46 @@ __device__ __forceinline__ void scan_bins_fixed(const uint32_t* hist, uint32_t n
       run += c[j];
     }
   }
+  group_sync<T>(bar_id);
+}
+
+// scan_bins_fixed that also stores, for every bin d, excl[d] = the number of
+// keys in the bins above d (thread-owned bins, 16-byte stores).
+template <int T, int NBINS>
+__device__ __forceinline__ void scan_bins_excl(const uint32_t* hist, uint32_t* excl, uint32_t need,
+                                               SelectShared& sh, int gtid, int bar_id) {
+  static_assert(NBINS % T == 0 && (NBINS / T) % 4 == 0, "whole 16-byte groups per thread");
+  constexpr int B = NBINS / T;
+  const int base = NBINS - (gtid + 1) * B;
+  uint32_t c[B];
+#pragma unroll
+  for (int j = 0; j < B; j += 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(hist + base + j);
+    c[j] = v.x;
+    c[j + 1] = v.y;
+    c[j + 2] = v.z;
+    c[j + 3] = v.w;
+  }
+  uint32_t local = 0;
+#pragma unroll
+  for (int j = 0; j < B; ++j) local += c[j];
+  uint32_t tot;
+  const uint32_t ex = group_excl_scan<T>(local, &tot, sh, gtid, bar_id);
+  uint32_t e[B];
+  uint32_t run = ex;
+#pragma unroll
+  for (int j = B - 1; j >= 0; --j) {
+    e[j] = run;
+    if (run < need && need <= run + c[j]) {
+      sh.digit = static_cast<uint32_t>(base + j);
+      sh.above = run;
+      sh.cnt = c[j];
+    }
+    run += c[j];
+  }
+#pragma unroll
+  for (int j = 0; j < B; j += 4)
+    *reinterpret_cast<uint4*>(excl + base + j) = make_uint4(e[j], e[j + 1], e[j + 2], e[j + 3]);
   group_sync<T>(bar_id);
 }
 
@@ -297,14 +338,17 @@ __device__ void select_row_regs(const uint32_t (&key)[R], int nb, int k, int32_t
 // key M: digit kSelHistBins-1-b holds the keys with (M - key) >> kSelWinShift
 // == b, for b < kSelHistBins - 1 (the 32 octaves of fp32 below M in steps of
 // 1/64 octave, wide enough to reach past a +1e9 tail score); keys further
-// below get digit 0 and are not counted. Score
-// rows are dense near their top, so the k-th largest key nearly always lies
-// in the window, in a bin of a few keys: one histogram and one scan finish
-// the search, and the boundary bin's keys are ranked directly. Otherwise
+// below get digit 0 and are not counted. Score rows are dense near their
+// top, so the k-th largest key nearly always lies in the window, in a bin of
+// a few keys: one histogram and one scan finish the search. The scan also
+// leaves each bin's output offset (the keys in higher bins), so winners are
+// scattered straight to their bin's slots and ordered inside the bin, and
+// the boundary bin's keys are ranked directly. Otherwise
 // (the k-th key below the window, or more than kSelBinMax keys in its bin)
 // the function returns false having written only hist and sh, and the
 // caller runs the fixed-digit select (select_row_regs). hist must be zero on
-// entry; keys past nb are 0.
+// entry; excl holds kSelHistBins words (16-byte aligned), sel_bin k words;
+// keys past nb are 0.
 constexpr int kSelWinShift = 17;
 
 // Loads keys already in shared memory into registers and zeroes hist (the
@@ -353,73 +397,105 @@ __device__ __forceinline__ void build_first_digit_hist(const uint32_t (&key)[R],
 
 template <int T, int R>
 __device__ bool select_row_window(const uint32_t (&key)[R], int nb, int k,
-                                  int32_t* __restrict__ out, uint32_t* hist, uint64_t* cand,
-                                  uint64_t* sel, SelectShared& sh, int gtid, int bar_id) {
+                                  int32_t* __restrict__ out, uint32_t* hist, uint32_t* excl,
+                                  uint64_t* cand, uint64_t* sel, uint32_t* sel_bin,
+                                  SelectShared& sh, int gtid, int bar_id) {
   constexpr int kWarps = T / 32;
   constexpr uint32_t kTop = kSelHistBins - 1;
   const int kk = k < nb ? k : nb;
-  uint32_t M = 0;
-  uint32_t bdig = 0;                      // the boundary digit
-  uint32_t need = static_cast<uint32_t>(kk);  // keys still needed from its bin
-  bool take_bin = true;                   // the boundary bin is taken whole
-  if (kk > 0 && kk < nb) {
+  if (kk < nb) {
     uint32_t m = 0;
 #pragma unroll
     for (int j = 0; j < R; ++j) m = max(m, key[j]);
     m = __reduce_max_sync(0xFFFFFFFFu, m);
     if ((gtid & 31) == 0) sh.wsum[gtid >> 5] = m;
-    if (gtid == 0) sh.cnt = 0xFFFFFFFFu;  // stays so unless the scan finds the digit
+    if (gtid == 0) {
+      sh.cnt = 0xFFFFFFFFu;  // stays so unless the scan finds the digit
+      sh.n_cand = 0;
+    }
     group_sync<T>(bar_id);
+    uint32_t M = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = max(M, sh.wsum[w]);
+    auto digit = [&](uint32_t kv) {
+      const uint32_t t = (M - kv) >> kSelWinShift;
+      return t < kTop ? kTop - t : 0u;
+    };
 #pragma unroll
     for (int j = 0; j < R; ++j) {
-      const uint32_t t = (M - key[j]) >> kSelWinShift;
-      if (j * T + gtid < nb && t < kTop) atomicAdd(&hist[kTop - t], 1u);
+      const uint32_t d = digit(key[j]);
+      if (j * T + gtid < nb && d > 0) atomicAdd(&hist[d], 1u);
     }
     group_sync<T>(bar_id);
-    scan_bins_fixed<T, kSelHistBins>(hist, need, sh, gtid, bar_id);
+    scan_bins_excl<T, kSelHistBins>(hist, excl, static_cast<uint32_t>(kk), sh, gtid, bar_id);
     const uint32_t cnt = sh.cnt;
     if (cnt == 0xFFFFFFFFu) return false;  // the k-th key lies below the window
-    bdig = sh.digit;
-    need -= sh.above;
-    take_bin = cnt == need;
+    const uint32_t bdig = sh.digit, above = sh.above;
+    const uint32_t need = static_cast<uint32_t>(kk) - above;
+    const bool take_bin = cnt == need;
     if (!take_bin && cnt > static_cast<uint32_t>(kSelBinMax)) return false;
-  }
 
-  if (kk > 0) {
-    uint32_t wmask = 0, cmask = 0;
+    // Winners (digits above the boundary, and the boundary bin when it is
+    // taken whole) go to a slot in their bin's output range [excl[d],
+    // excl[d-1]) (the boundary digit is at least 1: digit 0 is not counted);
+    // otherwise the boundary bin's keys become candidates.
 #pragma unroll
     for (int j = 0; j < R; ++j) {
-      const bool valid = j * T + gtid < nb;
-      const uint32_t t = (M - key[j]) >> kSelWinShift;
-      const uint32_t d = t < kTop ? kTop - t : 0u;
-      const bool w = valid && (kk == nb || d > bdig || (take_bin && d == bdig));
-      const bool c = valid && !take_bin && d == bdig;
-      wmask |= (w ? 1u : 0u) << j;
-      cmask |= (c ? 1u : 0u) << j;
-    }
-    uint32_t totals;
-    const uint32_t offs = group_excl_scan<T>((static_cast<uint32_t>(__popc(wmask)) << 16) |
-                                                 static_cast<uint32_t>(__popc(cmask)),
-                                             &totals, sh, gtid, bar_id);
-    uint32_t wo = offs >> 16, co = offs & 0xFFFFu;
-    const uint32_t n_win = totals >> 16, n_cand = totals & 0xFFFFu;
-#pragma unroll
-    for (int j = 0; j < R; ++j) {
-      if (wmask & (1u << j)) sel[wo++] = win_key(key[j], j * T + gtid);
-      if (cmask & (1u << j)) cand[co++] = win_key(key[j], j * T + gtid);
+      const uint32_t d = digit(key[j]);
+      if (j * T + gtid < nb && d >= bdig) {
+        const uint64_t wk = win_key(key[j], j * T + gtid);
+        if (d > bdig || take_bin) {
+          const uint32_t slot = excl[d] + atomicSub(&hist[d], 1u) - 1u;
+          sel[slot] = wk;
+          sel_bin[slot] = d;
+        } else {
+          cand[atomicAdd(&sh.n_cand, 1u)] = wk;
+        }
+      }
     }
     group_sync<T>(bar_id);
-    if (!take_bin) {
-      const uint32_t nd = need;
-      split_rank<T>(cand, static_cast<int>(n_cand), gtid, [&](int e, uint32_t r) {
-        if (r < nd) sel[n_win + r] = cand[e];
-      });
-      group_sync<T>(bar_id);
+    // Order inside each winner's bin (bins hold a few keys), P threads per
+    // winner, and the candidates' ranks: every output slot is written once.
+    const int n_win = static_cast<int>(take_bin ? static_cast<uint32_t>(kk) : above);
+    int P = 1;
+    while (P < 32 && 2 * P * n_win <= T) P <<= 1;
+    for (int b0 = 0; b0 < n_win * P; b0 += T) {
+      const int t = b0 + gtid, e = t / P, sub = t & (P - 1);
+      const bool valid = e < n_win;
+      uint64_t me = 0;
+      uint32_t lo = 0, r = 0;
+      if (valid) {
+        me = sel[e];
+        const uint32_t d = sel_bin[e];
+        lo = excl[d];
+        const uint32_t hi = excl[d - 1];
+        for (uint32_t i = lo + sub; i < hi; i += P) r += sel[i] > me ? 1u : 0u;
+      }
+      for (int o = 1; o < P; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
+      if (valid && sub == 0) out[lo + r] = static_cast<int32_t>(~static_cast<uint32_t>(me));
     }
+    if (!take_bin) {
+      const int n_c = static_cast<int>(cnt);
+      for (int e = gtid; e < n_c; e += T) {
+        const uint64_t me = cand[e];
+        uint32_t r = 0;
+        for (int i = 0; i < n_c; ++i) r += cand[i] > me ? 1u : 0u;
+        if (r < need) out[above + r] = static_cast<int32_t>(~static_cast<uint32_t>(me));
+      }
+    }
+    return true;
   }
 
+  // kk == nb: every key is a winner (and ids past nb are -1).
+  uint32_t wmask = 0;
+#pragma unroll
+  for (int j = 0; j < R; ++j) wmask |= (j * T + gtid < nb ? 1u : 0u) << j;
+  uint32_t n_win;
+  uint32_t wo = group_excl_scan<T>(static_cast<uint32_t>(__popc(wmask)), &n_win, sh, gtid, bar_id);
+#pragma unroll
+  for (int j = 0; j < R; ++j)
+    if (wmask & (1u << j)) sel[wo++] = win_key(key[j], j * T + gtid);
+  group_sync<T>(bar_id);
   split_rank<T>(sel, kk, gtid, [&](int e, uint32_t r) {
     out[r] = static_cast<int32_t>(~static_cast<uint32_t>(sel[e]));
   });
