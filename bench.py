@@ -46,8 +46,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # sources have changed since reports null. The capture and its command are
 # summarised in profiles/fused_step_kernel_long128k.md.
 NCU_TRAFFIC = {
-    "fused_step_kernel": {"bytes_per_launch": 1640960, "sources": ["fused.cu", "select_row.cuh"],
-                          "source_sha": "724c481832df3328",
+    "fused_step_kernel": {"bytes_per_launch": 1643264,
+                          "sources": ["fused.cu", "select_row.cuh", "qsa_device.cuh"],
+                          "source_sha": "2b76964414f25733",
                           "workload": "long128k_nq256_h8_d128_kv131072"},
 }
 
