@@ -187,3 +187,75 @@ def random_scores(nq: int, nb: int, seed: int, kind: str = "normal"):
     else:
         raise ValueError(kind)
     return np.ascontiguousarray(s.astype(np.float32))
+
+
+# ------------------------------------------------ flash-attention split reduce
+# Second workload: the reduce that closes a split (multi-block) flash-attention
+# decode (1bit-MONSTER llama.cpp pull request 30, "What" and "Changes": the
+# reduce_completed.multipass output pass). Per group g (one sequence and KV
+# head) and query row r (the query heads sharing that KV head), every KV block
+# b has left a block maximum of its scores, partial_max[g,r,b], the block's
+# sum of exp(score - that maximum), partial_sum[g,r,b], and the block's
+# unnormalised output over the value head, partial_out[g,r,b,c] (fp16).
+
+@dataclasses.dataclass(frozen=True)
+class SplitWorkload:
+    """G groups x R rows, B active blocks, C = value_head_size channels."""
+
+    name: str
+    G: int
+    R: int
+    B: int
+    C: int
+    seed: int
+
+
+SPLIT_WORKLOADS = [
+    # the multipass path's first depth past 2048 tokens (33 blocks of 64)
+    SplitWorkload("split_g2_r8_c128_b33", 2, 8, 33, 128, 2001),
+    # depth 4800 (76 blocks), the largest the page measured
+    SplitWorkload("split_g4_r8_c128_b76", 4, 8, 76, 128, 2002),
+    # 128K tokens (2048 blocks) at the production GQA shape
+    SplitWorkload("split_g4_r8_c128_b2048", 4, 8, 2048, 128, 2003),
+    # the review's worst staging case: 16 rows, 262,144 tokens (4096 blocks)
+    SplitWorkload("split_g2_r16_c128_b4096", 2, 16, 4096, 128, 2004),
+]
+SPLIT_BY_NAME = {w.name: w for w in SPLIT_WORKLOADS}
+
+
+def make_split_partials(w: SplitWorkload, variant: int = 0):
+    """Return (partial_max f32 [G,R,B], partial_sum f32 [G,R,B],
+    partial_out f16 [G,R,B,C]) drawn from a fixed recipe:
+
+      partial_max ~ N(0, 2), plus +6 on one drawn block per row (a dominant
+                    block, as an attention sink gives), so the per-block
+                    scales span many orders of magnitude;
+      partial_sum ~ U[1, 64] (a block of 64 tokens whose largest term is 1);
+      partial_out = partial_sum * N(0, 0.3) per channel, rounded to fp16.
+    """
+    rng = np.random.default_rng(w.seed + 104729 * variant)
+    pm = rng.normal(0.0, 2.0, size=(w.G, w.R, w.B))
+    hot = rng.integers(0, w.B, size=(w.G, w.R))
+    np.put_along_axis(pm, hot[..., None], np.take_along_axis(pm, hot[..., None], 2) + 6.0, 2)
+    ps = rng.uniform(1.0, 64.0, size=(w.G, w.R, w.B))
+    po = ps[..., None] * rng.normal(0.0, 0.3, size=(w.G, w.R, w.B, w.C))
+    return (np.ascontiguousarray(pm.astype(np.float32)),
+            np.ascontiguousarray(ps.astype(np.float32)), _f16(po))
+
+
+def split_random_case(G: int, R: int, B: int, C: int, seed: int, pm_sd: float = 2.0):
+    """Small plain cases of the same recipe (no dominant block)."""
+    rng = np.random.default_rng(seed)
+    pm = rng.normal(0.0, pm_sd, size=(G, R, B))
+    ps = rng.uniform(1.0, 64.0, size=(G, R, B))
+    po = ps[..., None] * rng.normal(0.0, 0.3, size=(G, R, B, C))
+    return (np.ascontiguousarray(pm.astype(np.float32)),
+            np.ascontiguousarray(ps.astype(np.float32)), _f16(po))
+
+
+def attention_scores_values(R: int, n_tokens: int, C: int, seed: int):
+    """Raw decode-attention operands for end-to-end checks of the reduce:
+    scores [R, n_tokens] ~ N(0, 3) (already scaled q.k) and values
+    [n_tokens, C] ~ N(0, 1), both float64."""
+    rng = np.random.default_rng(seed)
+    return rng.normal(0.0, 3.0, size=(R, n_tokens)), rng.normal(0.0, 1.0, size=(n_tokens, C))
