@@ -218,6 +218,46 @@ qsa_status qsa_select_step_host(const float* q32_host, const uint16_t* kb_host, 
                                 int32_t* ids_dev, qsa_stream_t stream);
 
 /*
+ * qsa_split_reduce - the flash-attention decode split reduce (a second
+ * workload: 1bit-MONSTER llama.cpp pull request 30, "What" and "Changes",
+ * the multipass reduce's output pass; its review's bounded scale stage).
+ * For each of G groups (a sequence and KV head) and R rows (the query heads
+ * sharing that KV head), B KV blocks have left partials; the call computes
+ *
+ *   maximum[r] = max_b partial_max[r,b]
+ *   scale[r,b] = exp(partial_max[r,b] - maximum[r])      once per (row, block)
+ *   sum[r]     = sum_b scale[r,b] * partial_sum[r,b]
+ *   out[r,c]   = (sum_b scale[r,b] * partial_out[r,b,c]) / sum[r]
+ *
+ *   partial_max, partial_sum  f32 [G, R, B] device, 4-byte aligned, finite.
+ *   partial_out               f16 [G, R, B, C] device, 8-byte aligned.
+ *   out                       f32 [G, R, C] device, 16-byte aligned.
+ *   workspace                 device, 16-byte aligned, at least
+ *                             qsa_split_reduce_workspace_bytes(G, R, B, C)
+ *                             bytes (0 when B <= 64: NULL allowed). Its first
+ *                             bytes hold arrival counters that must be zero
+ *                             before the first call (zero-fill it once); every
+ *                             call leaves them zero again. Calls that may run
+ *                             at the same time need separate workspaces.
+ * Arithmetic (fixed, so results are reproducible bit for bit on any GB300):
+ * the blocks are reduced in chunks of 64 (one CTA each, the scales of a
+ * chunk staged on chip); in a chunk, sum and out accumulate block by block
+ * in fp32, each term fl(scale * x) then one rounded add (no fused
+ * multiply-add); chunk partials are added in chunk order; out = fl(O / sum).
+ * exp is a fixed fp32 routine (Cody-Waite reduction, degree-7 Taylor
+ * polynomial; within 3 ulp of exp; arguments below -86 give 0).
+ * Supported: G >= 0 (0: nothing to do), 1 <= R <= 32, B >= 1, 4 <= C,
+ * C % 4 == 0, R * C <= 4096, G <= 65535.
+ * Errors: QSA_ERR_INVALID_ARG (a NULL buffer, B < 1, R < 1, G < 0, a
+ * workspace smaller than required), QSA_ERR_UNSUPPORTED_GEOMETRY, QSA_ERR_MISALIGNED.
+ */
+size_t qsa_split_reduce_workspace_bytes(int32_t G, int32_t R, int32_t B, int32_t C);
+qsa_status qsa_split_reduce(const float* partial_max, const float* partial_sum,
+                            const uint16_t* partial_out, int32_t G, int32_t R, int32_t B,
+                            int32_t C, float* out, void* workspace, size_t workspace_bytes,
+                            qsa_stream_t stream);
+
+/*
  * qsa_device_status - synchronizes `stream`, then reads the current device's
  * status word, where kernels record a bounded wait that ran out. Returns
  * QSA_OK if it is clear, QSA_ERR_TIMEOUT if not (and clears it when `clear`

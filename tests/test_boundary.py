@@ -141,6 +141,33 @@ def test_step_launches_host_rules(lib):
     assert n(4, 8, 128, 0, 64, 8, 1) == 0
 
 
+def test_split_reduce_host_rules(lib):
+    ws = lambda G, R, B, C: lib.qsa_split_reduce_workspace_bytes(G, R, B, C)
+    assert ws(4, 8, 64, 128) == 0                  # one chunk: no workspace
+    assert ws(0, 8, 2048, 128) == 0
+    # counters (16-byte padded), chunk sums, chunk outputs
+    assert ws(4, 8, 2048, 128) == 16 + 4 * 32 * 8 * 4 + 4 * 32 * 8 * 128 * 4
+    assert ws(3, 16, 65, 4) == 16 + 3 * 2 * 16 * 4 + 3 * 2 * 16 * 4 * 4
+    assert ws(1, 33, 100, 128) == 0                # unsupported: 33 rows
+    A = 1 << 20
+    v = ctypes.c_void_p
+    call = lambda G, R, B, C, pm=A, ps=A, po=A, out=A, w=A, wsz=1 << 30: lib.qsa_split_reduce(
+        v(pm), v(ps), v(po), G, R, B, C, v(out), v(w), wsz, None)
+    assert call(0, 8, 100, 128) == OK              # no groups: nothing to do
+    assert call(-1, 8, 100, 128) == INVALID
+    assert call(1, 0, 100, 128) == INVALID
+    assert call(1, 8, 0, 128) == INVALID
+    assert call(1, 33, 100, 128) == GEOM
+    assert call(1, 8, 100, 126) == GEOM            # C not a multiple of 4
+    assert call(1, 32, 100, 256) == GEOM           # R * C above 4096
+    assert call(1, 8, 100, 128, pm=0) == INVALID
+    assert call(1, 8, 100, 128, w=0) == INVALID    # two chunks need a workspace
+    assert call(1, 8, 100, 128, wsz=64) == INVALID
+    assert call(1, 8, 100, 128, po=A + 4) == MISALIGNED
+    assert call(1, 8, 100, 128, out=A + 8) == MISALIGNED
+    assert call(1, 8, 100, 128, w=A + 8) == MISALIGNED
+
+
 def test_selftest_rejects_bad_timeout_on_host(lib):
     assert lib.qsa_selftest_bounded_wait(0, None) == INVALID
     assert lib.qsa_selftest_bounded_wait(2_000_000_000, None) == INVALID

@@ -18,7 +18,7 @@ __all__ = [
     "qsa_num_blocks", "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select",
     "qsa_select_step", "qsa_select_step_host", "qsa_device_status", "qsa_selftest_bounded_wait",
     "qsa_select_step_batched", "qsa_score_select_batched", "qsa_select_step_launches",
-    "EXPORTED_SYMBOLS",
+    "qsa_split_reduce", "qsa_split_reduce_workspace_bytes", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,6 +30,7 @@ EXPORTED_SYMBOLS = (
     "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select", "qsa_select_step",
     "qsa_select_step_host", "qsa_device_status", "qsa_selftest_bounded_wait",
     "qsa_select_step_batched", "qsa_score_select_batched", "qsa_select_step_launches",
+    "qsa_split_reduce_workspace_bytes", "qsa_split_reduce",
 )
 
 STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED_GEOMETRY",
@@ -81,6 +82,9 @@ def load_library():
         "qsa_score_select_batched": (ctypes.c_int, [vp, vp, i64, i32, i32, i32, i32, i64, i32, i32,
                                                     vp, vp, vp]),
         "qsa_select_step_launches": (i32, [i32, i32, i32, i64, i32, i32, i32]),
+        "qsa_split_reduce_workspace_bytes": (ctypes.c_size_t, [i32, i32, i32, i32]),
+        "qsa_split_reduce": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, ctypes.c_size_t,
+                                            vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -393,3 +397,43 @@ def qsa_score_select_batched(q, kb, n_kv: int, k: int, block: int = 64, scores=N
                                             _ptr(scores), _ptr(ids), _stream_of(q)),
                "qsa_score_select_batched")
     return scores, ids
+
+
+# ------------------------------------------------------- split reduce
+def qsa_split_reduce_workspace_bytes(G: int, R: int, B: int, C: int) -> int:
+    """Bytes of workspace qsa_split_reduce needs (0 when B <= 64)."""
+    return int(load_library().qsa_split_reduce_workspace_bytes(G, R, B, C))
+
+
+def qsa_split_reduce(partial_max, partial_sum, partial_out, out=None, workspace=None):
+    """Flash-attention decode split reduce: partial_max / partial_sum f32
+    [G, R, B], partial_out f16 [G, R, B, C] -> out f32 [G, R, C].
+
+    workspace: a CUDA uint8 tensor of at least qsa_split_reduce_workspace_bytes
+    bytes whose counter area is zero (torch.zeros once; every call leaves it
+    zero). Allocated here when not given."""
+    torch = _torch()
+    _need(partial_max, torch.float32, 3, "partial_max")
+    _need(partial_sum, torch.float32, 3, "partial_sum")
+    _need(partial_out, torch.float16, 4, "partial_out")
+    G, R, B = partial_max.shape
+    C = partial_out.shape[3]
+    if tuple(partial_sum.shape) != (G, R, B) or tuple(partial_out.shape[:3]) != (G, R, B):
+        raise ValueError("partial_sum must be [G, R, B] and partial_out [G, R, B, C]")
+    dev = partial_max.device
+    if out is None:
+        out = torch.empty((G, R, C), dtype=torch.float32, device=dev)
+    _need(out, torch.float32, 3, "out")
+    if tuple(out.shape) != (G, R, C):
+        raise ValueError(f"out must be [{G}, {R}, {C}]")
+    lib = load_library()
+    with torch.cuda.device(dev):
+        need = int(lib.qsa_split_reduce_workspace_bytes(G, R, B, C))
+        if workspace is None:
+            workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
+        if workspace.dtype != torch.uint8 or not workspace.is_cuda or workspace.numel() < need:
+            raise ValueError(f"workspace must be a CUDA uint8 tensor of at least {need} bytes")
+        _check(lib.qsa_split_reduce(_ptr(partial_max), _ptr(partial_sum), _ptr(partial_out), G, R, B,
+                                    C, _ptr(out), _ptr(workspace), workspace.numel(),
+                                    _stream_of(partial_max)), "qsa_split_reduce")
+    return out

@@ -302,6 +302,40 @@ qsa_status qsa_select_step_host(const float* q32_host, const uint16_t* kb_host, 
   return QSA_OK;
 }
 
+// Shape rules of the split reduce; fills *ws with the workspace it needs.
+static qsa_status check_split(int32_t G, int32_t R, int32_t B, int32_t C, size_t* ws) {
+  if (G < 0 || R < 1 || B < 1 || C < 1) return QSA_ERR_INVALID_ARG;
+  if (R > qsa::kSrMaxRows || C % 4 != 0 || C < 4 || G > 65535 ||
+      static_cast<int64_t>(R) * C > 4LL * qsa::kSrMaxQuadsPerThread * 256)
+    return QSA_ERR_UNSUPPORTED_GEOMETRY;
+  *ws = qsa::split_reduce_workspace_bytes(G, R, B, C);
+  return QSA_OK;
+}
+
+size_t qsa_split_reduce_workspace_bytes(int32_t G, int32_t R, int32_t B, int32_t C) {
+  size_t ws = 0;
+  return check_split(G, R, B, C, &ws) == QSA_OK ? ws : 0;
+}
+
+qsa_status qsa_split_reduce(const float* partial_max, const float* partial_sum,
+                            const uint16_t* partial_out, int32_t G, int32_t R, int32_t B,
+                            int32_t C, float* out, void* workspace, size_t workspace_bytes,
+                            qsa_stream_t stream) {
+  size_t need = 0;
+  qsa_status st = check_split(G, R, B, C, &need);
+  if (st != QSA_OK) return st;
+  if (G == 0) return QSA_OK;
+  if (!partial_max || !partial_sum || !partial_out || !out) return QSA_ERR_INVALID_ARG;
+  if (need > 0 && (!workspace || workspace_bytes < need)) return QSA_ERR_INVALID_ARG;
+  if (!aligned(partial_max, 4) || !aligned(partial_sum, 4) || !aligned(partial_out, 8) ||
+      !aligned(out, 16) || (need > 0 && !aligned(workspace, 16)))
+    return QSA_ERR_MISALIGNED;
+  const DeviceInfo* dev = nullptr;
+  if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  qsa::SplitReduceProblem p{partial_max, partial_sum, partial_out, out, workspace, G, R, B, C};
+  return from_cuda(qsa::launch_split_reduce(p, *dev, as_cuda(stream)));
+}
+
 qsa_status qsa_selftest_bounded_wait(uint64_t timeout_ns, qsa_stream_t stream) {
   if (timeout_ns == 0 || timeout_ns > 1000000000ull) return QSA_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;

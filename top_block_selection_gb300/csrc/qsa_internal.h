@@ -97,6 +97,22 @@ cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k
 // Launches the bounded-wait self-test (see qsa_selftest_bounded_wait).
 cudaError_t launch_selftest_wait(const DeviceInfo& dev, uint64_t timeout_ns, cudaStream_t stream);
 
+// Flash-attention decode split reduce (split_reduce.cu).
+constexpr int kSrChunk = 64;              // blocks per CTA (the bounded scale stage)
+constexpr int kSrMaxRows = 32;            // rows (query heads per KV head)
+constexpr int kSrMaxQuadsPerThread = 4;   // R * C / 4 <= 4 * 256
+struct SplitReduceProblem {
+  const float* partial_max;
+  const float* partial_sum;
+  const uint16_t* partial_out;
+  float* out;
+  void* workspace;  // split_reduce_workspace_bytes(G, R, B, C) bytes; counters zero
+  int32_t G, R, B, C;
+};
+size_t split_reduce_workspace_bytes(int32_t G, int32_t R, int32_t B, int32_t C);
+cudaError_t launch_split_reduce(const SplitReduceProblem& p, const DeviceInfo& dev,
+                                cudaStream_t stream);
+
 constexpr int kMaxSelectK = 1024;
 constexpr int kMaxSelectNb = 32768;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s bound on any device-side wait
