@@ -65,6 +65,8 @@ def parse_args():
     p.add_argument("--min-timed-seconds", type=float, default=1.0,
                    help="repeat the K-step timed region until this much time has passed")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle baseline budget")
+    p.add_argument("--no-split", action="store_true",
+                   help="skip the split-reduce (second workload) measurement")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -419,6 +421,9 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
     }
+    if not args.no_split:
+        res["split_reduce"] = run_split(torch, tbs, device, stream, peaks, peak_src, K,
+                                        barrier if dist else None)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if rank == 0:
@@ -426,6 +431,57 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+SPLIT_WORKLOAD = "split_g4_r8_c128_b2048"
+
+
+def run_split(torch, tbs, device, stream, peaks, peak_src, K, barrier):
+    """The second workload, the flash-attention decode split reduce
+    (qsa_split_reduce), on its 128K-token shape: K calls in a CUDA graph over
+    rotating input sets larger than twice L2, one shared workspace. HBM-bound:
+    algorithmic bytes per call = partial_max + partial_sum + partial_out read
+    once, out written once."""
+    w = qi.SPLIT_BY_NAME[SPLIT_WORKLOAD]
+    per_set = 8 * w.G * w.R * w.B + 2 * w.G * w.R * w.B * w.C + 4 * w.G * w.R * w.C
+    n = max(4, -(-2 * L2_BYTES // per_set) + 1)
+    base = [tuple(torch.from_numpy(a).to(device) for a in qi.make_split_partials(w, variant=v))
+            for v in range(2)]
+    sets = [base[v % 2] if v < 2 else tuple(t.clone() for t in base[v % 2]) for v in range(n)]
+    outs = [torch.empty((w.G, w.R, w.C), dtype=torch.float32, device=device) for _ in range(n)]
+    need = tbs.qsa_split_reduce_workspace_bytes(w.G, w.R, w.B, w.C)
+    ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=device)
+
+    def call(i):
+        pm, ps, po = sets[i % n]
+        tbs.qsa_split_reduce(pm, ps, po, out=outs[i % n], workspace=ws)
+
+    with torch.cuda.stream(stream):
+        for i in range(4):
+            call(i)
+    torch.cuda.synchronize()
+    g = graph_of(torch, stream, call, K)
+
+    def replay():
+        with torch.cuda.stream(stream):
+            g.replay()
+    replay()
+    torch.cuda.synchronize()
+    ms = time_region(torch, stream, replay, 5, 0.5, barrier)
+    t = statistics.median(ms) / K / 1e3
+    algo = 8.0 * w.G * w.R * w.B + 2.0 * w.G * w.R * w.B * w.C + 4.0 * w.G * w.R * w.C
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return {
+        "workload": w.name, "G": w.G, "R": w.R, "B": w.B, "C": w.C,
+        "metric": "reduced (row, block) pairs/s", "value": world * w.G * w.R * w.B / t,
+        "us_per_call": t * 1e6, "launches_per_call": 1,
+        "roofline": {"bound": "hbm", "achieved": algo / t / 1e9, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": algo / t / 1e9 / peaks["hbm_gbs"],
+                     "traffic": traffic_for("split_reduce_kernel", w), "algorithmic_bytes": algo,
+                     "peak_source": peak_src},
+        "l2": f"rotating {n} input sets ({n * per_set / 2**20:.0f} MiB > 2x L2)",
+        "api": "qsa_split_reduce (CUDA graph of K calls)",
+    }
 
 
 def run_e2e(torch, tbs, w, device, stream, K, W, barrier, with_q16):

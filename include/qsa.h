@@ -234,16 +234,17 @@ qsa_status qsa_select_step_host(const float* q32_host, const uint16_t* kb_host, 
  *   out                       f32 [G, R, C] device, 16-byte aligned.
  *   workspace                 device, 16-byte aligned, at least
  *                             qsa_split_reduce_workspace_bytes(G, R, B, C)
- *                             bytes (0 when B <= 64: NULL allowed). Its first
+ *                             bytes (0 when B <= 128: NULL allowed). Its first
  *                             bytes hold arrival counters that must be zero
  *                             before the first call (zero-fill it once); every
  *                             call leaves them zero again. Calls that may run
  *                             at the same time need separate workspaces.
  * Arithmetic (fixed, so results are reproducible bit for bit on any GB300):
- * the blocks are reduced in chunks of 64 (one CTA each, the scales of a
- * chunk staged on chip); in a chunk, sum and out accumulate block by block
- * in fp32, each term fl(scale * x) then one rounded add (no fused
- * multiply-add); chunk partials are added in chunk order; out = fl(O / sum).
+ * the blocks are reduced in chunks of 128 (the scales of a chunk staged on
+ * chip), each chunk in runs of 32 blocks; in a run, sum and out accumulate
+ * block by block from 0 in fp32, each term fl(scale * x) then one rounded
+ * add (no fused multiply-add); a chunk's runs are added in order, then the
+ * chunk partials in chunk order; out = fl(O / sum).
  * exp is a fixed fp32 routine (Cody-Waite reduction, degree-7 Taylor
  * polynomial; within 3 ulp of exp; arguments below -86 give 0).
  * Supported: G >= 0 (0: nothing to do), 1 <= R <= 32, B >= 1, 4 <= C,

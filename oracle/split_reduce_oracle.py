@@ -34,11 +34,13 @@ Readings where the pages are silent (each also listed in the design notes):
   S1  Layouts: partial_max, partial_sum f32 [G, R, B]; partial_out f16
       [G, R, B, C] (C contiguous); out f32 [G, R, C].
   S2  The fp32 procedure is pinned (split_reduce_f32), in this order: the
-      blocks are taken in chunks of CHUNK = 64 (the bounded stage); inside a
-      chunk, sum and output accumulate block by block, each term rounded
-      (fl(scale * x)) and then added (no fused multiply-add); the chunk
-      partials are then added chunk by chunk; out = fl(O / sum). Every
-      operation is IEEE binary32 round-to-nearest-even.
+      blocks are taken in chunks of CHUNK = 128 (the bounded stage), each
+      chunk in runs of RUN = 32 consecutive blocks; inside a run, sum and
+      output accumulate block by block from 0, each term rounded
+      (fl(scale * x)) and then added (no fused multiply-add); a chunk's runs
+      are added in order from 0, then the chunk partials in chunk order from
+      0; out = fl(O / sum). Every operation is IEEE binary32
+      round-to-nearest-even. (Runs let four thread groups share a chunk.)
   S3  The scale's exponential is one pinned fp32 routine (exp_f32): Cody and
       Waite's range reduction exp(x) = 2^n exp(x - n ln 2), with ln 2 split
       into a 16-bit high part and a low part so that n * LN2_HI is exact,
@@ -59,7 +61,8 @@ import math
 
 import numpy as np
 
-CHUNK = 64  # S2: blocks per chunk (the fixed-size scale stage)
+CHUNK = 128  # S2: blocks per chunk (the fixed-size scale stage)
+RUN = 32     # S2: blocks per run inside a chunk
 
 # S3: Cody-Waite split of ln 2 (high part with 16 significant bits) and the
 # Taylor coefficients 1/k! for k = 7..0, all as float32.
@@ -113,10 +116,15 @@ def split_reduce_f32(pm, ps, po, chunk: int = CHUNK) -> np.ndarray:
     for b0 in range(0, B, chunk):
         part_s = np.zeros((G, R), np.float32)
         part_o = np.zeros((G, R, C), np.float32)
-        for b in range(b0, min(B, b0 + chunk)):
-            sc = scale[:, :, b]
-            part_s = part_s + sc * ps[:, :, b]
-            part_o = part_o + sc[..., None] * po32[:, :, b, :]
+        for r0 in range(b0, min(B, b0 + chunk), RUN):
+            run_s = np.zeros((G, R), np.float32)
+            run_o = np.zeros((G, R, C), np.float32)
+            for b in range(r0, min(B, r0 + RUN)):
+                sc = scale[:, :, b]
+                run_s = run_s + sc * ps[:, :, b]
+                run_o = run_o + sc[..., None] * po32[:, :, b, :]
+            part_s = part_s + run_s
+            part_o = part_o + run_o
         total_s = total_s + part_s
         total_o = total_o + part_o
     return (total_o / total_s[..., None]).astype(np.float32)
@@ -131,7 +139,7 @@ def error_bound(pm, ps, po, chunk: int = CHUNK) -> np.ndarray:
     scale is S (1 + e), |e| <= eta = |delta| u + 3 * 2^-23 (to first order),
     or exactly 0 where delta < -86 (an absolute loss of S <= e^-86). Each
     term fl(scale * x) adds u. Every sum is a tree of at most
-    h = chunk + ceil(B / chunk) additions along any path, so it adds at most
+    h = RUN + chunk / RUN + ceil(B / chunk) additions along any path, so it adds at most
     gamma_h = h u / (1 - h u) of the sum of the terms' magnitudes. Hence
     |dO| <= A = sum_b S_b |po_b| (eta_b + u + gamma_h) + flushed terms, and
     |dSum| <= sum * eps_s with eps_s the same weight on the (positive) sum
@@ -144,7 +152,7 @@ def error_bound(pm, ps, po, chunk: int = CHUNK) -> np.ndarray:
     po = np.asarray(po, np.float64)
     u = 2.0 ** -24
     B = pm.shape[2]
-    h = chunk + -(-B // chunk)
+    h = RUN + chunk // RUN + -(-B // chunk)
     gamma = h * u / (1.0 - h * u)
     maximum = pm.max(axis=2, keepdims=True)
     delta = pm - maximum

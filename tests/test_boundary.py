@@ -143,11 +143,11 @@ def test_step_launches_host_rules(lib):
 
 def test_split_reduce_host_rules(lib):
     ws = lambda G, R, B, C: lib.qsa_split_reduce_workspace_bytes(G, R, B, C)
-    assert ws(4, 8, 64, 128) == 0                  # one chunk: no workspace
+    assert ws(4, 8, 128, 128) == 0                 # one chunk: no workspace
     assert ws(0, 8, 2048, 128) == 0
-    # counters (16-byte padded), chunk sums, chunk outputs
-    assert ws(4, 8, 2048, 128) == 16 + 4 * 32 * 8 * 4 + 4 * 32 * 8 * 128 * 4
-    assert ws(3, 16, 65, 4) == 16 + 3 * 2 * 16 * 4 + 3 * 2 * 16 * 4 * 4
+    # counters (one per group and row, 16-byte padded), chunk sums, chunk outputs
+    assert ws(4, 8, 2048, 128) == 128 + 4 * 16 * 8 * 4 + 4 * 16 * 8 * 128 * 4
+    assert ws(3, 16, 129, 4) == 192 + 3 * 2 * 16 * 4 + 3 * 2 * 16 * 4 * 4
     assert ws(1, 33, 100, 128) == 0                # unsupported: 33 rows
     A = 1 << 20
     v = ctypes.c_void_p
@@ -161,11 +161,11 @@ def test_split_reduce_host_rules(lib):
     assert call(1, 8, 100, 126) == GEOM            # C not a multiple of 4
     assert call(1, 32, 100, 256) == GEOM           # R * C above 4096
     assert call(1, 8, 100, 128, pm=0) == INVALID
-    assert call(1, 8, 100, 128, w=0) == INVALID    # two chunks need a workspace
-    assert call(1, 8, 100, 128, wsz=64) == INVALID
+    assert call(1, 8, 200, 128, w=0) == INVALID    # two chunks need a workspace
+    assert call(1, 8, 200, 128, wsz=64) == INVALID
     assert call(1, 8, 100, 128, po=A + 4) == MISALIGNED
     assert call(1, 8, 100, 128, out=A + 8) == MISALIGNED
-    assert call(1, 8, 100, 128, w=A + 8) == MISALIGNED
+    assert call(1, 8, 200, 128, w=A + 8) == MISALIGNED
 
 
 def test_selftest_rejects_bad_timeout_on_host(lib):

@@ -104,7 +104,7 @@ def test_hand_example():
 
 # ------------------------------------------------------- the fp32 procedure
 CASES = [(1, 1, 1, 4), (2, 3, 5, 8), (1, 8, 63, 16), (1, 8, 64, 16), (2, 8, 65, 16),
-         (1, 4, 130, 128), (1, 16, 300, 32), (2, 8, 33, 128)]
+         (1, 4, 130, 128), (1, 16, 300, 32), (2, 8, 33, 128), (1, 2, 129, 8), (1, 3, 1000, 12)]
 
 
 @pytest.mark.parametrize("G,R,B,C", CASES)
@@ -164,4 +164,21 @@ def test_planted_reduce_mistakes_are_caught(monkeypatch):
 
 
 def test_chunk_count():
-    assert [sro.n_chunks(b) for b in (1, 64, 65, 2048, 4096)] == [1, 1, 2, 32, 64]
+    assert [sro.n_chunks(b) for b in (1, 128, 129, 2048, 4096)] == [1, 1, 2, 16, 32]
+
+
+def test_run_order_is_what_changes_the_bits():
+    """The pinned order is observable: on the same inputs a different run
+    length gives other fp32 bits (so the kernel must follow this one), while
+    both stay within the bound."""
+    pm, ps, po = qi.split_random_case(1, 4, 300, 64, seed=21)
+    a = sro.split_reduce_f32(pm, ps, po)
+    ref, bound = sro.split_reduce_f64(pm, ps, po), sro.error_bound(pm, ps, po)
+    old = sro.RUN
+    try:
+        sro.RUN = 128
+        b = sro.split_reduce_f32(pm, ps, po)
+    finally:
+        sro.RUN = old
+    assert not np.array_equal(a, b)
+    assert sro.bound_report(a, ref, bound)["ok"] and sro.bound_report(b, ref, bound)["ok"]

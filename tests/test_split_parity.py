@@ -46,7 +46,8 @@ def test_split_workloads(tbs, w):
 
 @pytest.mark.parametrize("G,R,B,C", [(1, 1, 1, 4), (3, 8, 1, 128), (2, 3, 63, 8), (1, 8, 64, 128),
                                      (2, 8, 65, 128), (1, 32, 129, 128), (3, 16, 300, 256),
-                                     (1, 5, 700, 12), (2, 8, 4097, 64), (1, 2, 5000, 4)])
+                                     (1, 5, 700, 12), (2, 8, 4097, 64), (1, 2, 5000, 4),
+                                     (1, 4, 200, 1024), (2, 32, 129, 128)])
 def test_split_shapes(tbs, G, R, B, C):
     pm, ps, po = qi.split_random_case(G, R, B, C, seed=G * 1000 + B)
     check(tbs, pm, ps, po, f"{G}x{R}x{B}x{C}")

@@ -13,6 +13,7 @@ enum : uint32_t {
   kErrScoreLoadTimeout = 1u << 0,  // TMA tile never arrived
   kErrScoreMmaTimeout = 1u << 1,   // tcgen05.commit never arrived
   kErrFusedWaitTimeout = 1u << 2,  // a cross-CTA dependency never completed
+  kErrSplitLoadTimeout = 1u << 3,  // a split-reduce bulk copy never arrived
   kErrSelftestTimeout = 1u << 31,  // the bounded-wait self-test ran out (expected)
 };
 
@@ -126,6 +127,24 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) 
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
                "r"(bytes)
                : "memory");
+}
+
+// Orders this thread's view of global memory (e.g. data acquired from other
+// CTAs) before its later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Contiguous bulk copy global -> this CTA's shared memory, completion as
+// transaction bytes on `bar`; both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // -------------------------------------------------------------- tcgen05

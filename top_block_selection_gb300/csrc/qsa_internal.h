@@ -98,9 +98,14 @@ cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k
 cudaError_t launch_selftest_wait(const DeviceInfo& dev, uint64_t timeout_ns, cudaStream_t stream);
 
 // Flash-attention decode split reduce (split_reduce.cu).
-constexpr int kSrChunk = 64;              // blocks per CTA (the bounded scale stage)
+constexpr int kSrChunk = 128;             // blocks per CTA (the bounded scale stage)
+constexpr int kSrRun = 32;                // blocks per run inside a chunk
+constexpr int kSrRuns = kSrChunk / kSrRun;
 constexpr int kSrMaxRows = 32;            // rows (query heads per KV head)
 constexpr int kSrMaxQuadsPerThread = 4;   // R * C / 4 <= 4 * 256
+constexpr int kSrStageBytes = 96 * 1024;  // staged fp16 partial outputs per CTA
+constexpr int kSrSmemMax =
+    kSrStageBytes + kSrRuns * 1024 * 16 + kSrRuns * kSrMaxRows * 4 + 2 * kSrMaxRows * kSrChunk * 4;
 struct SplitReduceProblem {
   const float* partial_max;
   const float* partial_sum;
@@ -110,6 +115,7 @@ struct SplitReduceProblem {
   int32_t G, R, B, C;
 };
 size_t split_reduce_workspace_bytes(int32_t G, int32_t R, int32_t B, int32_t C);
+cudaError_t init_split_reduce_kernel(const DeviceInfo& dev);
 cudaError_t launch_split_reduce(const SplitReduceProblem& p, const DeviceInfo& dev,
                                 cudaStream_t stream);
 

@@ -7,21 +7,26 @@
 // partial_sum_b; out[c] = (sum_b scale_b * partial_out_b[c]) / sum.
 //
 // GB300 layout of the work: the blocks are cut into chunks of kSrChunk
-// (64); CTA (j, g) reduces chunk j of group g. Each CTA finds the rows'
-// maxima over all blocks (partial_max is small and L2-resident), stages its
-// chunk's scales in shared memory (R x 64 floats: bounded whatever the
-// context length), and runs the all-rows output pass: a thread owns a quad
-// of 4 channels of one row and accumulates fp32 over the chunk's blocks from
-// 8-byte fp16 loads (a warp reads 256 contiguous bytes per block). Chunk
-// partials go to the caller's workspace; the last CTA of a group to finish
-// (an arrival counter) adds them in chunk order and divides. With one chunk
-// the CTA writes the output directly.
+// (128) and a group's rows into splits of Rs rows; CTA (chunk, split, group)
+// bulk-copies its rows' fp16 partial outputs for the chunk into shared
+// memory (when the rows are 16-byte aligned), finds the rows' maxima over all
+// blocks meanwhile (partial_max is small and L2-resident), stages the
+// chunk's scales and partial sums (bounded whatever the context length), and
+// runs the all-rows output pass: a work item is a quad of 4 channels of one
+// row over one run of kSrRun blocks (four runs per chunk keep all warps
+// busy). Chunk partials go to the caller's workspace; the last CTA of a
+// (group, split) to finish (an arrival counter) bulk-copies them back and
+// adds them in chunk order, then divides. With one chunk the CTA writes the
+// output directly.
 //
 // Arithmetic, fixed operation for operation (the CPU oracle's pinned fp32
 // procedure follows the same steps): scale = exp_pinned(fl(pm - maximum));
-// inside a chunk, acc = fl(acc + fl(scale * x)) block by block (no fused
-// multiply-add); chunk partials added in chunk order; out = fl(O / sum).
+// inside a run, acc = fl(acc + fl(scale * x)) block by block from 0 (no
+// fused multiply-add); a chunk's runs added in order from 0; chunk partials
+// added in chunk order from 0; out = fl(O / sum).
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
@@ -59,50 +64,185 @@ struct SrArgs {
   const float* ps;      // [G][R][B]
   const __half* po;     // [G][R][B][C]
   float* out;           // [G][R][C]
-  uint32_t* count;      // [G] arrival counters (zero between calls)
+  uint32_t* count;      // [G][R] arrival counters, one per (group, row split); zero between calls
   float* part_sum;      // [G][S][R]
   float* part_out;      // [G][S][R][C]
+  uint32_t* status;     // device status word (bounded-wait failures)
+  uint64_t timeout_ns;
   int R, B, C, S;
+  int RS, Rs;           // row splits per group, rows per split
+  int staged;           // 1: the chunk's partial outputs are staged by bulk copies
+  int pm_vec;           // 1: partial_max and partial_sum rows are 16-byte aligned
+  int stage_bytes;      // dynamic shared memory before the run partials
 };
 
 __global__ void __launch_bounds__(kSrThreads) split_reduce_kernel(const SrArgs a) {
+  // [Rs][kSrChunk][C] fp16 when staged (stage_bytes), then the run partials
+  extern __shared__ __align__(128) uint8_t sr_stage[];
   __shared__ float s_max[kSrMaxRows];
+  __shared__ float s_part[kSrMaxRows];
   __shared__ float s_rowsum[kSrMaxRows];
-  __shared__ float s_scale[kSrMaxRows * kSrChunk];
-  __shared__ int s_last;
-  const int j = blockIdx.x, g = blockIdx.y;
+
+  __shared__ __align__(8) uint64_t bar_stage;
+  __shared__ int s_last, s_ok;
+  const int j = blockIdx.x, rs = blockIdx.y, g = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = a.R, B = a.B, C = a.C;
+  const int r0 = rs * a.Rs;
+  const int nr = min(a.Rs, R - r0);  // rows of this CTA
   const int64_t grb = static_cast<int64_t>(g) * R * B;
-
-  pdl_launch_dependents();
-  pdl_wait();
-
-  // Row maxima over every block (one warp per row).
-  for (int r = warp; r < R; r += kSrThreads / 32) {
-    const float* row = a.pm + grb + static_cast<int64_t>(r) * B;
-    float m = __int_as_float(0xff800000u);  // -inf
-    for (int b = lane; b < B; b += 32) m = fmaxf(m, __ldg(row + b));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if (lane == 0) s_max[r] = m;
-  }
-  __syncthreads();
-
-  // This chunk's scales, staged per row.
   const int b0 = j * kSrChunk;
   const int nbk = min(kSrChunk, B - b0);
-  for (int i = tid; i < R * nbk; i += kSrThreads) {
+  const uint32_t row_bytes = static_cast<uint32_t>(nbk) * C * 2u;
+  // Dynamic shared memory: [stage_bytes of staged partial outputs]
+  // [run partials kSrRuns x quads float4][run sums kSrRuns x Rs]
+  // [scales Rs x kSrChunk][partial sums Rs x kSrChunk].
+  const int nquads_max = a.Rs * (C / 4);
+  float4* run_out = reinterpret_cast<float4*>(sr_stage + a.stage_bytes);
+  float* run_sum = reinterpret_cast<float*>(run_out + kSrRuns * nquads_max);
+  float* s_scale = run_sum + kSrRuns * a.Rs;
+  float* s_psum = s_scale + a.Rs * kSrChunk;
+
+  pdl_launch_dependents();
+  if (tid == 0) {
+    if (a.staged) {
+      mbar_init(&bar_stage, 1);
+      fence_mbarrier_init();
+      // The chunk's partial outputs on their way to L2 while the previous
+      // kernel finishes (a hint; the copies proper come after the wait).
+      for (int r = 0; r < nr; ++r)
+        bulk_prefetch_l2(a.po + (grb + static_cast<int64_t>(r0 + r) * B + b0) * C, row_bytes);
+    }
+    if (a.pm_vec) {
+      // the rows' maxima inputs and this chunk's partial sums (whole 16-byte
+      // pieces; a hint only)
+      for (int r = 0; r < nr; ++r) {
+        const int64_t row = grb + static_cast<int64_t>(r0 + r) * B;
+        bulk_prefetch_l2(a.pm + row, static_cast<uint32_t>(B) * 4u);
+        const uint32_t ps_bytes = (static_cast<uint32_t>(nbk) * 4u) & ~15u;
+        if (ps_bytes) bulk_prefetch_l2(a.ps + row + b0, ps_bytes);
+      }
+    }
+  }
+  pdl_wait();
+  if (a.staged && tid == 0) {
+    mbar_arrive_expect_tx(&bar_stage, row_bytes * static_cast<uint32_t>(nr));
+    for (int r = 0; r < nr; ++r)
+      bulk_load(sr_stage + static_cast<size_t>(r) * kSrChunk * C * 2,
+                a.po + (grb + static_cast<int64_t>(r0 + r) * B + b0) * C, row_bytes, &bar_stage);
+  }
+
+  // Row maxima over every block, while the copies fly: the CTA's warps
+  // split its rows (several warps per row when there are fewer than 8),
+  // 16-byte loads when the rows allow, many loads in flight per lane.
+  {
+    constexpr int kWarps = kSrThreads / 32;
+    const int wpr = nr < kWarps ? kWarps / nr : 1;
+    const float ninf = __int_as_float(0xff800000u);
+    for (int task = warp; task < nr * wpr; task += kWarps) {
+      const int r = task / wpr, part = task - r * wpr;
+      const float* row = a.pm + grb + static_cast<int64_t>(r0 + r) * B;
+      float m = ninf;
+      if (a.pm_vec) {
+        const int n4 = B / 4, len = (n4 + wpr - 1) / wpr;
+        const float4* row4 = reinterpret_cast<const float4*>(row);
+        const int hi = min(n4, (part + 1) * len);
+#pragma unroll 8
+        for (int i = part * len + lane; i < hi; i += 32) {
+          const float4 v = __ldg(row4 + i);
+          m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+        }
+      } else {
+        const int len = (B + wpr - 1) / wpr;
+        const int hi = min(B, (part + 1) * len);
+#pragma unroll 8
+        for (int b = part * len + lane; b < hi; b += 32) m = fmaxf(m, __ldg(row + b));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+      if (lane == 0) s_part[task] = m;
+    }
+    __syncthreads();
+    if (tid < nr) {
+      float m = ninf;
+      for (int p = 0; p < wpr; ++p) m = fmaxf(m, s_part[tid * wpr + p]);
+      s_max[tid] = m;
+    }
+    __syncthreads();
+  }
+
+  // This chunk's scales and partial sums, staged per row.
+  for (int i = tid; i < nr * nbk; i += kSrThreads) {
     const int r = i / nbk, bl = i - r * nbk;
-    const float d = __fsub_rn(__ldg(a.pm + grb + static_cast<int64_t>(r) * B + b0 + bl), s_max[r]);
-    s_scale[r * kSrChunk + bl] = exp_pinned(d);
+    const int64_t at = grb + static_cast<int64_t>(r0 + r) * B + b0 + bl;
+    const float pmv = __ldg(a.pm + at);
+    s_psum[r * kSrChunk + bl] = __ldg(a.ps + at);
+    s_scale[r * kSrChunk + bl] = exp_pinned(__fsub_rn(pmv, s_max[r]));
+  }
+  if (tid == 0) s_ok = a.staged ? mbar_wait_bounded(&bar_stage, 0, a.timeout_ns) : 1;
+  __syncthreads();
+  if (!s_ok) {
+    // The copies never completed: record it, give them one more bounded
+    // wait so none lands after the CTA has gone, and leave (no output; the
+    // workspace counters must be zeroed again before the next call).
+    if (tid == 0) {
+      atomicOr(a.status, kErrSplitLoadTimeout);
+      mbar_wait_bounded(&bar_stage, 0, a.timeout_ns);
+    }
+    return;
+  }
+
+  // Output pass. Work item = (run of kSrRun blocks, quad of 4 channels of a
+  // row); consecutive threads take consecutive quads (256 contiguous bytes
+  // per warp and block). A run accumulates from 0 block by block; the quad
+  // at channel 0 also accumulates the row's sum. Run partials go to shared
+  // memory and are then added in run order.
+  const int qpr = C / 4;
+  const int nquads = nr * qpr;
+  const int nruns = (nbk + kSrRun - 1) / kSrRun;
+  const int stride = C / 4;  // uint2 (4 halves) per block
+  for (int item = tid; item < nruns * nquads; item += kSrThreads) {
+    const int run = item / nquads, q = item - run * nquads;
+    const int r = q / qpr, c = (q - r * qpr) * 4;
+    const int bl_lo = run * kSrRun, bl_hi = min(nbk, bl_lo + kSrRun);
+    const float* srow = s_scale + r * kSrChunk;
+    const float* psrow = s_psum + r * kSrChunk;
+    float o0 = 0.0f, o1 = 0.0f, o2 = 0.0f, o3 = 0.0f, acc_s = 0.0f;
+    if (a.staged) {
+      const uint2* src = reinterpret_cast<const uint2*>(sr_stage) +
+                         static_cast<size_t>(r) * kSrChunk * stride + c / 4;
+#pragma unroll 8
+      for (int bl = bl_lo; bl < bl_hi; ++bl) {
+        const uint2 v = src[bl * stride];
+        const float sc = srow[bl];
+        const __half2 h01 = *reinterpret_cast<const __half2*>(&v.x);
+        const __half2 h23 = *reinterpret_cast<const __half2*>(&v.y);
+        o0 = __fadd_rn(o0, __fmul_rn(sc, __low2float(h01)));
+        o1 = __fadd_rn(o1, __fmul_rn(sc, __high2float(h01)));
+        o2 = __fadd_rn(o2, __fmul_rn(sc, __low2float(h23)));
+        o3 = __fadd_rn(o3, __fmul_rn(sc, __high2float(h23)));
+        if (c == 0) acc_s = __fadd_rn(acc_s, __fmul_rn(sc, psrow[bl]));
+      }
+    } else {
+      const uint2* src = reinterpret_cast<const uint2*>(
+          a.po + ((grb + static_cast<int64_t>(r0 + r) * B + b0) * C + c));
+#pragma unroll 8
+      for (int bl = bl_lo; bl < bl_hi; ++bl) {
+        const uint2 v = __ldg(src + bl * stride);
+        const float sc = srow[bl];
+        const __half2 h01 = *reinterpret_cast<const __half2*>(&v.x);
+        const __half2 h23 = *reinterpret_cast<const __half2*>(&v.y);
+        o0 = __fadd_rn(o0, __fmul_rn(sc, __low2float(h01)));
+        o1 = __fadd_rn(o1, __fmul_rn(sc, __high2float(h01)));
+        o2 = __fadd_rn(o2, __fmul_rn(sc, __low2float(h23)));
+        o3 = __fadd_rn(o3, __fmul_rn(sc, __high2float(h23)));
+        if (c == 0) acc_s = __fadd_rn(acc_s, __fmul_rn(sc, psrow[bl]));
+      }
+    }
+    run_out[run * nquads + q] = make_float4(o0, o1, o2, o3);
+    if (c == 0) run_sum[run * nr + r] = acc_s;
   }
   __syncthreads();
-
-  // Output pass: thread -> quads (row, 4 channels); the quad at channel 0
-  // also accumulates the row's sum.
-  const int qpr = C / 4;
-  const int nquads = R * qpr;
   float acc_q[kSrMaxQuadsPerThread][4];
   float acc_sq[kSrMaxQuadsPerThread];
 #pragma unroll
@@ -111,46 +251,19 @@ __global__ void __launch_bounds__(kSrThreads) split_reduce_kernel(const SrArgs a
     acc_sq[u] = 0.0f;
     const int q = tid + u * kSrThreads;
     if (q >= nquads) continue;
-    const int r = q / qpr, c = (q - r * qpr) * 4;
-    const uint2* src = reinterpret_cast<const uint2*>(
-        a.po + ((grb + static_cast<int64_t>(r) * B + b0) * C + c));
-    const float* srow = s_scale + r * kSrChunk;
-    const float* psrow = a.ps + grb + static_cast<int64_t>(r) * B + b0;
-    const int64_t stride = C / 4;  // uint2 (4 halves) per block
-    float o0 = 0.0f, o1 = 0.0f, o2 = 0.0f, o3 = 0.0f, acc_s = 0.0f;
-    for (int bl0 = 0; bl0 < nbk; bl0 += 8) {
-      uint2 v[8];
-      float pv[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (bl0 + e < nbk) {
-          v[e] = __ldg(src + (bl0 + e) * stride);
-          pv[e] = c == 0 ? __ldg(psrow + bl0 + e) : 0.0f;
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (bl0 + e < nbk) {
-          const float s = srow[bl0 + e];
-          const __half2 h01 = *reinterpret_cast<const __half2*>(&v[e].x);
-          const __half2 h23 = *reinterpret_cast<const __half2*>(&v[e].y);
-          o0 = __fadd_rn(o0, __fmul_rn(s, __low2float(h01)));
-          o1 = __fadd_rn(o1, __fmul_rn(s, __high2float(h01)));
-          o2 = __fadd_rn(o2, __fmul_rn(s, __low2float(h23)));
-          o3 = __fadd_rn(o3, __fmul_rn(s, __high2float(h23)));
-          if (c == 0) acc_s = __fadd_rn(acc_s, __fmul_rn(s, pv[e]));
-        }
-      }
+    const int r = q / qpr, c = q - r * qpr;
+    for (int run = 0; run < nruns; ++run) {
+      const float4 v = run_out[run * nquads + q];
+      acc_q[u][0] = __fadd_rn(acc_q[u][0], v.x);
+      acc_q[u][1] = __fadd_rn(acc_q[u][1], v.y);
+      acc_q[u][2] = __fadd_rn(acc_q[u][2], v.z);
+      acc_q[u][3] = __fadd_rn(acc_q[u][3], v.w);
+      acc_sq[u] = __fadd_rn(acc_sq[u], run_sum[run * nr + r]);
     }
-    acc_q[u][0] = o0;
-    acc_q[u][1] = o1;
-    acc_q[u][2] = o2;
-    acc_q[u][3] = o3;
-    acc_sq[u] = acc_s;
-    if (c == 0) s_rowsum[r] = acc_s;
+    if (c == 0) s_rowsum[r] = acc_sq[u];
   }
 
-  const int64_t grc = static_cast<int64_t>(g) * R * C;
+  const int64_t grc = (static_cast<int64_t>(g) * R + r0) * C;
   if (a.S == 1) {
     // One chunk: its partials are the totals (0 + x is exact).
     __syncthreads();
@@ -168,41 +281,119 @@ __global__ void __launch_bounds__(kSrThreads) split_reduce_kernel(const SrArgs a
   }
 
   // Several chunks: publish this chunk's partials, then the last CTA of the
-  // group adds them in chunk order.
+  // (group, row split) adds them in chunk order.
   const int64_t gs = static_cast<int64_t>(g) * a.S;
 #pragma unroll
   for (int u = 0; u < kSrMaxQuadsPerThread; ++u) {
     const int q = tid + u * kSrThreads;
     if (q >= nquads) continue;
     const int r = q / qpr, c = (q - r * qpr) * 4;
-    *reinterpret_cast<float4*>(a.part_out + ((gs + j) * R + r) * C + c) =
+    *reinterpret_cast<float4*>(a.part_out + ((gs + j) * R + r0 + r) * C + c) =
         make_float4(acc_q[u][0], acc_q[u][1], acc_q[u][2], acc_q[u][3]);
-    if (c == 0) a.part_sum[(gs + j) * R + r] = acc_sq[u];
+    if (c == 0) a.part_sum[(gs + j) * R + r0 + r] = acc_sq[u];
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.count + g, 1u) == static_cast<uint32_t>(a.S - 1);
+  uint32_t* counter = a.count + static_cast<int64_t>(g) * R + rs;
+  if (tid == 0) s_last = atomicAdd(counter, 1u) == static_cast<uint32_t>(a.S - 1);
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  if (tid == 0) a.count[g] = 0;  // ready for the next call
+  if (tid == 0) *counter = 0;  // ready for the next call
+#pragma unroll
+  for (int u = 0; u < kSrMaxQuadsPerThread; ++u) {
+    acc_q[u][0] = acc_q[u][1] = acc_q[u][2] = acc_q[u][3] = 0.0f;
+    acc_sq[u] = 0.0f;
+  }
+  const int64_t jstride = static_cast<int64_t>(R) * C;  // floats between chunks
+  if (a.staged) {
+    // The chunk partials of this CTA's rows, staged by bulk copies in rounds
+    // that fill the staging buffer, added in chunk order.
+    fence_proxy_async_global();  // peers' partials, acquired above, seen by the copies
+    const uint32_t slice = static_cast<uint32_t>(nr) * C * 4u;  // one chunk's rows
+    const int per_round = static_cast<int>(static_cast<uint32_t>(a.stage_bytes) / slice);
+    float* stage = reinterpret_cast<float*>(sr_stage);
+    for (int j0 = 0, round = 1; j0 < a.S; j0 += per_round, ++round) {
+      const int nj = min(per_round, a.S - j0);
+      if (tid == 0) {
+        // the stage was last read through the generic proxy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(&bar_stage, slice * static_cast<uint32_t>(nj));
+        for (int jj = 0; jj < nj; ++jj)
+          bulk_load(stage + static_cast<size_t>(jj) * nr * C,
+                    a.part_out + ((gs + j0 + jj) * R + r0) * C, slice, &bar_stage);
+      }
+      for (int i = tid; i < nj * nr; i += kSrThreads) {
+        const int jj = i / nr, r = i - jj * nr;
+        s_psum[i] = __ldcg(a.part_sum + (gs + j0 + jj) * R + r0 + r);  // nj * nr <= 64 * Rs
+      }
+      if (tid == 0) s_ok = mbar_wait_bounded(&bar_stage, round & 1, a.timeout_ns);
+      __syncthreads();
+      if (!s_ok) {
+        if (tid == 0) {
+          atomicOr(a.status, kErrSplitLoadTimeout);
+          mbar_wait_bounded(&bar_stage, round & 1, a.timeout_ns);
+        }
+        return;
+      }
+#pragma unroll
+      for (int u = 0; u < kSrMaxQuadsPerThread; ++u) {
+        const int q = tid + u * kSrThreads;
+        if (q >= nquads) continue;
+        const int r = q / qpr, c = (q - r * qpr) * 4;
+        for (int jj = 0; jj < nj; ++jj) {
+          const float4 v = *reinterpret_cast<const float4*>(stage + (static_cast<size_t>(jj) * nr + r) * C + c);
+          acc_sq[u] = __fadd_rn(acc_sq[u], s_psum[jj * nr + r]);
+          acc_q[u][0] = __fadd_rn(acc_q[u][0], v.x);
+          acc_q[u][1] = __fadd_rn(acc_q[u][1], v.y);
+          acc_q[u][2] = __fadd_rn(acc_q[u][2], v.z);
+          acc_q[u][3] = __fadd_rn(acc_q[u][3], v.w);
+        }
+      }
+      __syncthreads();  // the stage is refilled by the next round
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kSrMaxQuadsPerThread; ++u) {
+      const int q = tid + u * kSrThreads;
+      if (q >= nquads) continue;
+      const int r = q / qpr, c = (q - r * qpr) * 4;
+      const float4* po4 = reinterpret_cast<const float4*>(a.part_out + (gs * R + r0 + r) * C + c);
+      const float* psum = a.part_sum + gs * R + r0 + r;
+#pragma unroll 16
+      for (int jj = 0; jj < a.S; ++jj) {
+        const float4 v = __ldcg(po4 + jj * (jstride / 4));
+        acc_sq[u] = __fadd_rn(acc_sq[u], __ldcg(psum + static_cast<int64_t>(jj) * R));
+        acc_q[u][0] = __fadd_rn(acc_q[u][0], v.x);
+        acc_q[u][1] = __fadd_rn(acc_q[u][1], v.y);
+        acc_q[u][2] = __fadd_rn(acc_q[u][2], v.z);
+        acc_q[u][3] = __fadd_rn(acc_q[u][3], v.w);
+      }
+    }
+  }
 #pragma unroll
   for (int u = 0; u < kSrMaxQuadsPerThread; ++u) {
     const int q = tid + u * kSrThreads;
     if (q >= nquads) continue;
     const int r = q / qpr, c = (q - r * qpr) * 4;
-    float L = 0.0f, o0 = 0.0f, o1 = 0.0f, o2 = 0.0f, o3 = 0.0f;
-    for (int jj = 0; jj < a.S; ++jj) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_out + ((gs + jj) * R + r) * C + c));
-      L = __fadd_rn(L, __ldcg(a.part_sum + (gs + jj) * R + r));
-      o0 = __fadd_rn(o0, v.x);
-      o1 = __fadd_rn(o1, v.y);
-      o2 = __fadd_rn(o2, v.z);
-      o3 = __fadd_rn(o3, v.w);
-    }
+    const float L = acc_sq[u];
     *reinterpret_cast<float4*>(a.out + grc + static_cast<int64_t>(r) * C + c) =
-        make_float4(__fdiv_rn(o0, L), __fdiv_rn(o1, L), __fdiv_rn(o2, L), __fdiv_rn(o3, L));
+        make_float4(__fdiv_rn(acc_q[u][0], L), __fdiv_rn(acc_q[u][1], L),
+                    __fdiv_rn(acc_q[u][2], L), __fdiv_rn(acc_q[u][3], L));
   }
+}
+
+// Rows per CTA: the whole chunk of a CTA's rows must fit one staging buffer,
+// and the grid should cover the GPU about twice.
+void split_rows(int32_t G, int32_t R, int32_t B, int32_t C, int sm_count, int* RS, int* Rs) {
+  const int64_t S = (static_cast<int64_t>(B) + kSrChunk - 1) / kSrChunk;
+  const int64_t row_chunk = static_cast<int64_t>(kSrChunk) * C * 2;
+  int rows = static_cast<int>(std::max<int64_t>(1, kSrStageBytes / row_chunk));
+  rows = std::min(rows, static_cast<int>(R));
+  const int64_t want = 2LL * sm_count;
+  while (rows > 1 && static_cast<int64_t>(G) * S * ((R + rows - 1) / rows) < want) rows = (rows + 1) / 2;
+  *Rs = rows;
+  *RS = (R + rows - 1) / rows;
 }
 
 }  // namespace
@@ -210,14 +401,19 @@ __global__ void __launch_bounds__(kSrThreads) split_reduce_kernel(const SrArgs a
 size_t split_reduce_workspace_bytes(int32_t G, int32_t R, int32_t B, int32_t C) {
   const int64_t S = (static_cast<int64_t>(B) + kSrChunk - 1) / kSrChunk;
   if (G <= 0 || S <= 1) return 0;
-  const size_t counters = (static_cast<size_t>(G) * sizeof(uint32_t) + 15) & ~static_cast<size_t>(15);
+  const size_t counters = (static_cast<size_t>(G) * R * sizeof(uint32_t) + 15) & ~static_cast<size_t>(15);
   const size_t sums = (static_cast<size_t>(G) * S * R * sizeof(float) + 15) & ~static_cast<size_t>(15);
   return counters + sums + static_cast<size_t>(G) * S * R * C * sizeof(float);
 }
 
+cudaError_t init_split_reduce_kernel(const DeviceInfo& dev) {
+  (void)dev;
+  return cudaFuncSetAttribute(split_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSrSmemMax);
+}
+
 cudaError_t launch_split_reduce(const SplitReduceProblem& p, const DeviceInfo& dev,
                                 cudaStream_t stream) {
-  (void)dev;
   if (p.G <= 0) return cudaSuccess;
   SrArgs a;
   a.pm = p.partial_max;
@@ -228,14 +424,32 @@ cudaError_t launch_split_reduce(const SplitReduceProblem& p, const DeviceInfo& d
   a.B = p.B;
   a.C = p.C;
   a.S = (p.B + kSrChunk - 1) / kSrChunk;
+  a.status = dev.status_word;
+  a.timeout_ns = kWaitTimeoutNs;
+  split_rows(p.G, p.R, p.B, p.C, dev.sm_count, &a.RS, &a.Rs);
+  // Bulk copies need 16-byte aligned rows (C a multiple of 8 and an aligned
+  // base), and one row's chunk must fit the staging buffer (C <= 768).
+  a.staged = (p.C % 8 == 0 && reinterpret_cast<uintptr_t>(p.partial_out) % 16 == 0 &&
+              static_cast<int64_t>(kSrChunk) * p.C * 2 <= kSrStageBytes)
+                 ? 1 : 0;
+  a.pm_vec = (p.B % 4 == 0 && reinterpret_cast<uintptr_t>(p.partial_max) % 16 == 0 &&
+              reinterpret_cast<uintptr_t>(p.partial_sum) % 16 == 0)
+                 ? 1 : 0;
+  a.stage_bytes = a.staged ? a.Rs * kSrChunk * p.C * 2 : 0;
+  const size_t smem = static_cast<size_t>(a.stage_bytes) +
+                      static_cast<size_t>(kSrRuns) * (a.Rs * p.C / 4) * 16 +
+                      static_cast<size_t>(kSrRuns) * a.Rs * 4 +
+                      2 * static_cast<size_t>(a.Rs) * kSrChunk * 4;
   uint8_t* ws = static_cast<uint8_t*>(p.workspace);
-  const size_t counters = (static_cast<size_t>(p.G) * sizeof(uint32_t) + 15) & ~static_cast<size_t>(15);
+  const size_t counters = (static_cast<size_t>(p.G) * p.R * sizeof(uint32_t) + 15) & ~static_cast<size_t>(15);
   const size_t sums = (static_cast<size_t>(p.G) * a.S * p.R * sizeof(float) + 15) & ~static_cast<size_t>(15);
   a.count = a.S > 1 ? reinterpret_cast<uint32_t*>(ws) : nullptr;
   a.part_sum = a.S > 1 ? reinterpret_cast<float*>(ws + counters) : nullptr;
   a.part_out = a.S > 1 ? reinterpret_cast<float*>(ws + counters + sums) : nullptr;
-  return launch_pdl(split_reduce_kernel, dim3(static_cast<unsigned>(a.S), static_cast<unsigned>(p.G)),
-                    dim3(kSrThreads), 0, stream, a);
+  return launch_pdl(split_reduce_kernel,
+                    dim3(static_cast<unsigned>(a.S), static_cast<unsigned>(a.RS),
+                         static_cast<unsigned>(p.G)),
+                    dim3(kSrThreads), smem, stream, a);
 }
 
 }  // namespace qsa
