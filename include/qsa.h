@@ -259,6 +259,32 @@ qsa_status qsa_split_reduce(const float* partial_max, const float* partial_sum,
                             qsa_stream_t stream);
 
 /*
+ * qsa_split_reduce_static - qsa_split_reduce without a caller workspace, for
+ * callers that cannot allocate device memory at call time (a serving loop
+ * that must stay out of the allocator, whose cudaMalloc / cudaFree
+ * synchronise the device; a plain C host without a caching allocator). The
+ * pages have no counterpart of this entry point: it is library plumbing, not
+ * part of the method.
+ *
+ * Same arguments (less the workspace) and bit-identical results. The chunk
+ * partials and arrival counters live in one fixed array of
+ * QSA_SPLIT_STATIC_SCRATCH_BYTES per device inside the library; nothing is
+ * allocated. Shapes whose qsa_split_reduce_workspace_bytes exceeds it
+ * return QSA_ERR_UNSUPPORTED_GEOMETRY without a launch.
+ * Every call first clears the array's counter area on `stream` (an
+ * asynchronous memset, no allocation), then launches the reduce.
+ * Calls that may run at the same time on one device (other streams or other
+ * host threads) share the array and race: serialise them.
+ * The first call on each device looks up the array's address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture on the device.
+ */
+#define QSA_SPLIT_STATIC_SCRATCH_BYTES (4u << 20)
+qsa_status qsa_split_reduce_static(const float* partial_max, const float* partial_sum,
+                                   const uint16_t* partial_out, int32_t G, int32_t R, int32_t B,
+                                   int32_t C, float* out, qsa_stream_t stream);
+
+/*
  * qsa_device_status - synchronizes `stream`, then reads the current device's
  * status word, where kernels record a bounded wait that ran out. Returns
  * QSA_OK if it is clear, QSA_ERR_TIMEOUT if not (and clears it when `clear`

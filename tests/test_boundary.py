@@ -168,6 +168,18 @@ def test_split_reduce_host_rules(lib):
     assert call(1, 8, 200, 128, w=A + 8) == MISALIGNED
 
 
+def test_split_reduce_static_host_rules(lib):
+    A = 1 << 20
+    v = ctypes.c_void_p
+    call = lambda G, R, B, C, pm=A, out=A: lib.qsa_split_reduce_static(v(pm), v(A), v(A), G, R, B, C,
+                                                                      v(out), None)
+    assert call(0, 8, 2048, 128) == OK                 # no groups
+    assert call(64, 8, 4096, 128) == GEOM              # needs more than the fixed 4 MiB
+    assert call(1, 33, 100, 128) == GEOM
+    assert call(1, 8, 300, 128, pm=0) == INVALID
+    assert call(1, 8, 300, 128, out=A + 8) == MISALIGNED
+
+
 def test_selftest_rejects_bad_timeout_on_host(lib):
     assert lib.qsa_selftest_bounded_wait(0, None) == INVALID
     assert lib.qsa_selftest_bounded_wait(2_000_000_000, None) == INVALID

@@ -30,7 +30,7 @@ EXPORTED_SYMBOLS = (
     "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select", "qsa_select_step",
     "qsa_select_step_host", "qsa_device_status", "qsa_selftest_bounded_wait",
     "qsa_select_step_batched", "qsa_score_select_batched", "qsa_select_step_launches",
-    "qsa_split_reduce_workspace_bytes", "qsa_split_reduce",
+    "qsa_split_reduce_workspace_bytes", "qsa_split_reduce", "qsa_split_reduce_static",
 )
 
 STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED_GEOMETRY",
@@ -85,6 +85,7 @@ def load_library():
         "qsa_split_reduce_workspace_bytes": (ctypes.c_size_t, [i32, i32, i32, i32]),
         "qsa_split_reduce": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp, ctypes.c_size_t,
                                             vp]),
+        "qsa_split_reduce_static": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -336,6 +336,34 @@ qsa_status qsa_split_reduce(const float* partial_max, const float* partial_sum,
   return from_cuda(qsa::launch_split_reduce(p, *dev, as_cuda(stream)));
 }
 
+qsa_status qsa_split_reduce_static(const float* partial_max, const float* partial_sum,
+                                   const uint16_t* partial_out, int32_t G, int32_t R, int32_t B,
+                                   int32_t C, float* out, qsa_stream_t stream) {
+  size_t need = 0;
+  qsa_status st = check_split(G, R, B, C, &need);
+  if (st != QSA_OK) return st;
+  if (need > QSA_SPLIT_STATIC_SCRATCH_BYTES) return QSA_ERR_UNSUPPORTED_GEOMETRY;
+  if (G == 0) return QSA_OK;
+  if (!partial_max || !partial_sum || !partial_out || !out) return QSA_ERR_INVALID_ARG;
+  if (!aligned(partial_max, 4) || !aligned(partial_sum, 4) || !aligned(partial_out, 8) ||
+      !aligned(out, 16))
+    return QSA_ERR_MISALIGNED;
+  const DeviceInfo* dev = nullptr;
+  if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  cudaError_t e = cudaSuccess;
+  void* scratch = qsa::split_static_scratch(&e);
+  if (!scratch) return cuda_fail(e);
+  cudaStream_t s = as_cuda(stream);
+  if (need > 0) {
+    // The counters lead the workspace layout and must be zero; an earlier
+    // call of another shape may have left partials where they now sit.
+    const size_t counters = (static_cast<size_t>(G) * R * sizeof(uint32_t) + 15) & ~static_cast<size_t>(15);
+    if ((e = cudaMemsetAsync(scratch, 0, counters, s)) != cudaSuccess) return cuda_fail(e);
+  }
+  qsa::SplitReduceProblem p{partial_max, partial_sum, partial_out, out, scratch, G, R, B, C};
+  return from_cuda(qsa::launch_split_reduce(p, *dev, s));
+}
+
 qsa_status qsa_selftest_bounded_wait(uint64_t timeout_ns, qsa_stream_t stream) {
   if (timeout_ns == 0 || timeout_ns > 1000000000ull) return QSA_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;

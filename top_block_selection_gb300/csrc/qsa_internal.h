@@ -116,6 +116,10 @@ struct SplitReduceProblem {
 };
 size_t split_reduce_workspace_bytes(int32_t G, int32_t R, int32_t B, int32_t C);
 cudaError_t init_split_reduce_kernel(const DeviceInfo& dev);
+// Address of the current device's fixed split-reduce scratch
+// (QSA_SPLIT_STATIC_SCRATCH_BYTES), looked up once per device; null and *err
+// set on failure.
+void* split_static_scratch(cudaError_t* err);
 cudaError_t launch_split_reduce(const SplitReduceProblem& p, const DeviceInfo& dev,
                                 cudaStream_t stream);
 
