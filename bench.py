@@ -43,13 +43,17 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by kernel, with the SHA-256 (first 16 hex
 # digits) of the kernel's source files at capture time; an entry whose
-# sources have changed since reports null. The capture and its command are
-# summarised in profiles/fused_step_kernel_long128k.md.
+# sources have changed since reports null. The captures and their commands
+# are summarised in profiles/.
 NCU_TRAFFIC = {
     "fused_step_kernel": {"bytes_per_launch": 1643264,
                           "sources": ["fused.cu", "select_row.cuh", "qsa_device.cuh"],
                           "source_sha": "2b76964414f25733",
                           "workload": "long128k_nq256_h8_d128_kv131072"},
+    "split_reduce_kernel": {"bytes_per_launch": 17387264,
+                            "sources": ["split_reduce.cu", "qsa_device.cuh", "qsa_internal.h"],
+                            "source_sha": "a09571c947151937",
+                            "workload": "split_g4_r8_c128_b2048"},
 }
 
 
