@@ -158,20 +158,43 @@ class ClockSampler:
 
 
 # -------------------------------------------------------------- GPU helpers
+def rank_variants(rank, n):
+    """The input-set variants rank `rank` draws: every rank processes its own
+    independent query batches (weak scaling, no collective on the data)."""
+    return range(rank * n, rank * n + n)
+
+
+def max_over_ranks(torch, dist, value, device):
+    """The largest of `value` over all ranks (the timing rule); `value` itself
+    when there is one rank."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(world, units_per_rank, ms):
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 class Sets:
     """Rotating device buffer sets for one workload, stored as contiguous
     [n, ...] tensors so that a slice of consecutive sets is itself a batch."""
 
-    def __init__(self, torch, tbs, w, device, min_bytes):
+    def __init__(self, torch, tbs, w, device, min_bytes, rank=0):
         per = (w.nq * w.H * w.D * (4 + 2) + w.nb * w.D * 2 + w.nq * w.nb * 4 + w.nq * w.k * 4)
         n = max(2, math.ceil(min_bytes / per))
         self.n = ((n + 7) // 8) * 8  # whole groups of 8 for the batched launch
         self.per_set_bytes = per
+        self.variants = rank_variants(rank, self.n)
         self.q32 = torch.empty((self.n, w.nq, w.H, w.D), dtype=torch.float32, device=device)
         self.kb = torch.empty((self.n, w.nb, w.D), dtype=torch.float16, device=device)
-        for v in range(self.n):
-            q32, _ = qi.make_f32_inputs(w, variant=v)
-            _, kb = qi.make_inputs(w, variant=v)
+        for v, var in enumerate(self.variants):
+            q32, _ = qi.make_f32_inputs(w, variant=var)
+            _, kb = qi.make_inputs(w, variant=var)
             self.q32[v].copy_(torch.from_numpy(q32))
             self.kb[v].copy_(torch.from_numpy(kb))
         self.q16 = torch.empty((self.n, w.nq, w.H, w.D), dtype=torch.float16, device=device)
@@ -256,9 +279,7 @@ def run_ours(args):
         if ms is None:
             dist.barrier()
             return None
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(torch, dist, ms, device)
 
     if rank == 0:
         _build.build()
@@ -270,7 +291,7 @@ def run_ours(args):
     K, W = args.steps, args.warmup
     if K < 1 or W < 3:
         raise SystemExit("need --steps >= 1 and --warmup >= 3")
-    sets = Sets(torch, tbs, w, device, 2 * L2_BYTES)
+    sets = Sets(torch, tbs, w, device, 2 * L2_BYTES, rank)
     stream = torch.cuda.Stream(device)
     peaks, peak_src = load_peaks()
 
@@ -349,7 +370,7 @@ def run_ours(args):
     batched_ms = time_region(torch, stream, replays["batched"], 5, 0.5, barrier if dist else None)
 
     ms_step = statistics.median(step_ms) / K
-    value = world * units_per_step(w) * K / (statistics.median(step_ms) / 1e3)
+    value = aggregate_rate(world, units_per_step(w) * K, statistics.median(step_ms))
 
     # The step's roofline: one launch of the fused kernel (or, for a problem
     # too large for it, the chain of separate kernels, taken as a whole).
