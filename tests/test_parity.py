@@ -190,6 +190,24 @@ def test_large_step_paths_agree(tbs):
     assert tbs.qsa_select_step_launches(h.nq, h.H, h.D, h.n_kv, h.k, h.block, with_q16=True) == 1
 
 
+@pytest.mark.parametrize("nq,H,n_kv", [(1000, 8, 2500 * 64 + 5), (600, 16, 1900 * 64)])
+def test_large_scorer_ragged(tbs, nq, H, n_kv):
+    """Shapes large enough for the persistent score kernel (many 128 x 256
+    tiles), ragged in both directions: qsa_block_scores within the bound,
+    the tail bitwise, and bit for bit with the fused kernel's scores."""
+    q, kb = qi.random_case(nq, H, 128, -(-n_kv // 64), seed=nq + H, scale=0.25)
+    qd, kd = dev(q), dev(kb)
+    s_p = tbs.qsa_block_scores(qd, kd, n_kv, 64)
+    s_f, _ = tbs.qsa_score_select_batched(qd[None], kd, n_kv, 8, 64)
+    torch.cuda.synchronize()
+    assert torch.equal(s_p.view(torch.int32), s_f[0].view(torch.int32))
+    s = s_p.cpu().numpy()
+    s_ref, S, B, tail = orc.reference_scores(q, kb, n_kv, 64)
+    assert orc.bound_report(s, s_ref, B)["ok"]
+    if tail is not None:
+        assert s[:, -1].view(np.uint32).tolist() == tail.view(np.uint32).tolist()
+
+
 def test_select_step_without_q16_output(tbs):
     w = qi.WORKLOADS[0]
     q32, _ = qi.make_f32_inputs(w)

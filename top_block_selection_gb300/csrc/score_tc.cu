@@ -155,6 +155,214 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (warp == 0) tmem_dealloc(tmem_d, a.tmem_cols);
 }
 
+// ------------------------------------------------- persistent variant
+// For problems of many tiles: one CTA per SM walks a contiguous run of tiles
+// in m-fastest order (so the query tile changes rarely), with warp roles:
+// warp 8 lane 0 issues the TMA loads (kb tiles into a 3-stage ring, the query
+// tile when the run moves to the next column tile), warp 9 lane 0 issues the
+// MMAs into two TMEM accumulators, and warps 0-7 (two per TMEM lane quarter,
+// one column half each, four 32-column TMEM loads in flight) drain an
+// accumulator with the same ReLU / head-sum epilogue, in the same order,
+// while the next tile's MMAs run. Each score is computed exactly as by
+// score_tc_kernel.
+constexpr int kPStages = 3;
+constexpr int kPEpiWarps = 8;                   // two per TMEM lane quarter
+constexpr int kPThreads = 32 * (kPEpiWarps + 2);  // + TMA producer + MMA issuer
+constexpr int kPProducerWarp = kPEpiWarps, kPMmaWarp = kPEpiWarps + 1;
+
+__device__ __forceinline__ void mbar_arrive_local(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+struct PersistArgs {
+  int64_t m_tiles, tiles;  // tiles = m_tiles * n_tiles
+};
+
+template <int H>
+__global__ void __launch_bounds__(kPThreads, 1)
+    score_tc_persistent_kernel(const __grid_constant__ CUtensorMap tm_kb,
+                               const __grid_constant__ CUtensorMap tm_q, const ScoreArgs a,
+                               const PersistArgs pa) {
+  static_assert(32 % H == 0, "a 32-column TMEM load must hold whole queries");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const int a_bytes = a.n_chunks * kTileM * kRowBytes;  // one kb stage
+  uint8_t* sQ = smem;                                    // n_chunks x [bn rows x 128 B]
+  uint8_t* sA = sQ + a.n_chunks * a.bn * kRowBytes;      // kPStages kb stages
+  __shared__ uint64_t full[kPStages], empty[kPStages], acc_full[2], acc_empty[2], q_full, q_free;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int failed;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // This CTA's contiguous run of tiles [t0, t1).
+  const int64_t per = pa.tiles / gridDim.x, extra = pa.tiles % gridDim.x;
+  const int64_t bx = blockIdx.x;
+  const int64_t t0 = bx * per + (bx < extra ? bx : extra);
+  const int64_t count = per + (blockIdx.x < extra ? 1 : 0);
+
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], 32 * kPEpiWarps);
+    }
+    mbar_init(&q_full, 1);
+    mbar_init(&q_free, 1);
+    failed = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tm_kb);
+    tma_prefetch_desc(&tm_q);
+  }
+  if (warp == kPProducerWarp) {
+    tmem_alloc(&tmem_slot, 2u * a.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = tmem_slot;
+  pdl_wait();  // q and kb may come from the previous kernel on the stream
+
+  if (warp == kPProducerWarp) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int64_t cur_n = -1, issued = 0;
+      uint32_t qf_phase = 0, q_loads_issued_phase = 0;
+      const uint32_t q_bytes = static_cast<uint32_t>(a.n_chunks * a.bn * kRowBytes);
+      for (int64_t i = 0; i < count && !failed; ++i) {
+        const int64_t t = t0 + i, n = t / pa.m_tiles, m = t - n * pa.m_tiles;
+        if (n != cur_n) {
+          if (cur_n >= 0) {  // every MMA on the previous query tile has completed
+            if (!mbar_wait_bounded(&q_free, qf_phase, a.timeout_ns)) { failed = 1; break; }
+            qf_phase ^= 1u;
+          }
+          if (cur_n >= 0) q_loads_issued_phase ^= 1u;  // phase of the load issued now
+          mbar_arrive_expect_tx(&q_full, q_bytes);
+          for (int c = 0; c < a.n_chunks; ++c)
+            tma_load_2d(sQ + c * a.bn * kRowBytes, &tm_q, c * kKAtom, static_cast<int32_t>(n * a.bn),
+                        &q_full);
+          cur_n = n;
+        }
+        const int s = static_cast<int>(i % kPStages);
+        const int64_t use = i / kPStages;
+        if (use > 0 && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((use - 1) & 1), a.timeout_ns)) {
+          failed = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(a_bytes));
+        for (int c = 0; c < a.n_chunks; ++c)
+          tma_load_2d(sA + s * a_bytes + c * kTileM * kRowBytes, &tm_kb, c * kKAtom,
+                      static_cast<int32_t>(m * kTileM), &full[s]);
+        issued = i + 1;
+      }
+      if (failed) {
+        // Loads may still be in flight into shared memory: wait for the last
+        // ones issued (bounded) before the CTA may finish.
+        atomicOr(a.status, kErrScoreLoadTimeout);
+        for (int64_t j = issued > kPStages ? issued - kPStages : 0; j < issued; ++j)
+          mbar_wait_bounded(&full[j % kPStages], static_cast<uint32_t>((j / kPStages) & 1), a.timeout_ns);
+        if (cur_n >= 0) mbar_wait_bounded(&q_full, q_loads_issued_phase, a.timeout_ns);
+      }
+    }
+  } else if (warp == kPMmaWarp) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(kTileM, a.bn);
+      int64_t cur_n = -1;
+      uint32_t q_phase = 0;
+      for (int64_t i = 0; i < count && !failed; ++i) {
+        const int64_t t = t0 + i, n = t / pa.m_tiles;
+        if (n != cur_n) {
+          if (cur_n >= 0) mma_commit(&q_free);  // fires when the old tile's MMAs are done
+          if (!mbar_wait_bounded(&q_full, q_phase, a.timeout_ns)) { failed = 1; break; }
+          q_phase ^= 1u;
+          cur_n = n;
+        }
+        const int s = static_cast<int>(i % kPStages);
+        const int acc = static_cast<int>(i & 1);
+        if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((i / kPStages) & 1), a.timeout_ns)) {
+          failed = 1;
+          break;
+        }
+        if (i >= 2 && !mbar_wait_bounded(&acc_empty[acc], static_cast<uint32_t>(((i >> 1) - 1) & 1),
+                                         a.timeout_ns)) {
+          failed = 1;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * a.tmem_cols;
+        for (int c = 0; c < a.n_chunks; ++c) {
+          const uint32_t a_base = smem_u32(sA + s * a_bytes + c * kTileM * kRowBytes);
+          const uint32_t b_base = smem_u32(sQ + c * a.bn * kRowBytes);
+#pragma unroll
+          for (int ks = 0; ks < kKAtom / 16; ++ks) {
+            const int step = c * (kKAtom / 16) + ks;
+            if (step < a.k_steps)
+              mma_f16_ss(d_tmem, smem_desc_k_sw128(a_base + ks * 32),
+                         smem_desc_k_sw128(b_base + ks * 32), idesc, step > 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(&empty[s]);
+        mma_commit(&acc_full[acc]);
+      }
+      if (failed) atomicOr(a.status, kErrScoreMmaTimeout);
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 0-7)
+    const int lane_base = (warp & 3) * 32;
+    const int half_cols = a.bn >> 1;
+    const int c_begin = (warp >> 2) * half_cols;
+    constexpr int kQPerLoad = 32 / H;
+    for (int64_t i = 0; i < count; ++i) {
+      const int acc = static_cast<int>(i & 1);
+      if (failed || !mbar_wait_bounded(&acc_full[acc], static_cast<uint32_t>((i >> 1) & 1), a.timeout_ns)) {
+        failed = 1;
+        break;
+      }
+      tc_fence_after_sync();
+      const int64_t t = t0 + i, n = t / pa.m_tiles, m = t - n * pa.m_tiles;
+      const int b = static_cast<int>(m) * kTileM + lane_base + lane;
+      const bool b_ok = b < a.n_full;
+      float* out = a.scores + b;
+      const int q0 = static_cast<int>(n) * a.q_per_tile;
+      const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc) * a.tmem_cols +
+                             (static_cast<uint32_t>(lane_base) << 16);
+      for (int cb = c_begin; cb < c_begin + half_cols; cb += 128) {
+        // up to four 32-column loads in flight, then one wait
+        const int nld = min(4, (c_begin + half_cols - cb) / 32);
+        uint32_t r[4][32];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (u < nld) tmem_ld_32cols(taddr + cb + u * 32, r[u]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (u >= nld) continue;
+          const int c0 = cb + u * 32;
+#pragma unroll
+          for (int j = 0; j < kQPerLoad; ++j) {
+            float sc = 0.0f;
+#pragma unroll
+            for (int h = 0; h < H; ++h) sc = __fadd_rn(sc, fmaxf(__uint_as_float(r[u][j * H + h]), 0.0f));
+            const int qidx = q0 + c0 / H + j;
+            if (b_ok && qidx < a.nq) out[static_cast<size_t>(qidx) * a.nb] = sc;
+          }
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive_local(&acc_empty[acc]);
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kPProducerWarp) tmem_dealloc(tmem_base, 2u * a.tmem_cols);
+}
+
 __global__ void __launch_bounds__(kTailThreads)
     tail_kernel(const __half* __restrict__ q, const __half* __restrict__ kb_tail,
                 float* __restrict__ scores, int32_t nq, int32_t H, int32_t D, int64_t nb) {
@@ -214,6 +422,23 @@ const void* score_kernel_ptr() {
   return reinterpret_cast<const void*>(&score_tc_kernel<H>);
 }
 
+template <int H>
+const void* persistent_kernel_ptr() {
+  return reinterpret_cast<const void*>(&score_tc_persistent_kernel<H>);
+}
+
+const void* persistent_kernel_for(int H) {
+  switch (H) {
+    case 1: return persistent_kernel_ptr<1>();
+    case 2: return persistent_kernel_ptr<2>();
+    case 4: return persistent_kernel_ptr<4>();
+    case 8: return persistent_kernel_ptr<8>();
+    case 16: return persistent_kernel_ptr<16>();
+    case 32: return persistent_kernel_ptr<32>();
+    default: return nullptr;
+  }
+}
+
 const void* score_kernel_for(int H) {
   switch (H) {
     case 1: return score_kernel_ptr<1>();
@@ -254,12 +479,14 @@ int choose_bn(int64_t m_tiles, int64_t cols, int sm_count) {
 
 cudaError_t init_score_kernels(const DeviceInfo& dev) {
   for (int H : {1, 2, 4, 8, 16, 32}) {
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, score_kernel_for(H));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(score_kernel_for(H), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             dev.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
-    if (e != cudaSuccess) return e;
+    for (const void* fn : {score_kernel_for(H), persistent_kernel_for(H)}) {
+      cudaFuncAttributes fa;
+      cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dev.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
+      if (e != cudaSuccess) return e;
+    }
   }
   return cudaSuccess;
 }
@@ -287,6 +514,35 @@ cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStre
     a.tmem_cols = tmem_cols_for(bn);
     a.status = dev.status_word;
     a.timeout_ns = kWaitTimeoutNs;
+    // Many full-width tiles: the persistent kernel (one CTA per SM, pipelined
+    // loads, MMAs and epilogue); the same arithmetic per score.
+    const size_t psmem = static_cast<size_t>(a.n_chunks) * (bn + kPStages * kTileM) * kRowBytes + 1024;
+    if (bn == 256 && m_tiles * n_tiles >= 4LL * dev.sm_count &&
+        psmem <= static_cast<size_t>(dev.max_smem_optin) - 1024) {
+      PersistArgs pa{m_tiles, m_tiles * n_tiles};
+      const dim3 pgrid(static_cast<unsigned>(std::min<int64_t>(dev.sm_count, pa.tiles)));
+      const dim3 pblock(kPThreads);
+      cudaError_t e = cudaErrorInvalidValue;
+      switch (p.H) {
+        case 1: e = launch_pdl(score_tc_persistent_kernel<1>, pgrid, pblock, psmem, stream, tm_kb, tm_q, a, pa); break;
+        case 2: e = launch_pdl(score_tc_persistent_kernel<2>, pgrid, pblock, psmem, stream, tm_kb, tm_q, a, pa); break;
+        case 4: e = launch_pdl(score_tc_persistent_kernel<4>, pgrid, pblock, psmem, stream, tm_kb, tm_q, a, pa); break;
+        case 8: e = launch_pdl(score_tc_persistent_kernel<8>, pgrid, pblock, psmem, stream, tm_kb, tm_q, a, pa); break;
+        case 16: e = launch_pdl(score_tc_persistent_kernel<16>, pgrid, pblock, psmem, stream, tm_kb, tm_q, a, pa); break;
+        case 32: e = launch_pdl(score_tc_persistent_kernel<32>, pgrid, pblock, psmem, stream, tm_kb, tm_q, a, pa); break;
+        default: break;
+      }
+      if (e != cudaSuccess) return e;
+      if (p.nq > 0 && p.has_tail) {
+        const int q_per_block = kTailThreads / p.H;
+        const int64_t grid = (p.nq + q_per_block - 1) / q_per_block;
+        return launch_pdl(tail_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTailThreads), 0,
+                          stream, reinterpret_cast<const __half*>(p.q),
+                          reinterpret_cast<const __half*>(p.kb) + (p.nb - 1) * p.D, p.scores,
+                          p.nq, p.H, p.D, p.nb);
+      }
+      return cudaSuccess;
+    }
     const size_t smem = score_smem_bytes(bn, a.n_chunks, a.tmem_cols);
     if (smem > static_cast<size_t>(dev.max_smem_optin)) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(m_tiles), static_cast<unsigned>(n_tiles));
