@@ -134,6 +134,15 @@ def random_case(nq: int, H: int, D: int, nb: int, seed: int, scale: float = 1.0)
     return _f16(q), _f16(kb)
 
 
+def random_case_f32(nq: int, H: int, D: int, nb: int, seed: int, scale: float = 1.0):
+    """N(0, scale) q [nq,H,D] as f32 (the input of the fp32->fp16 stage) and
+    kb [nb,D] as fp16."""
+    rng = np.random.default_rng(seed)
+    q = rng.normal(0.0, scale, size=(nq, H, D))
+    kb = rng.normal(0.0, scale, size=(nb, D))
+    return np.ascontiguousarray(q.astype(np.float32)), _f16(kb)
+
+
 def coordinate_coded_case(nq: int, H: int, D: int, nb: int):
     """Coordinate-coded fixture: kb[b] = e_(b mod D) (one-hot, value 1) and
     q[qi,h,i] = ((7*qi + 3*h + i) mod 61) - 30, small integers exact in fp16.

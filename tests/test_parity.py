@@ -339,6 +339,40 @@ def test_select_step_from_f32(tbs, w):
     assert np.array_equal(ids_gpu.cpu().numpy(), orc.select_topk(s, w.k))
 
 
+@pytest.mark.parametrize("nq,H,D,nb,tail", [(1, 8, 128, 129, True), (9, 8, 128, 129, False),
+                                          (17, 8, 128, 63, True), (129, 8, 128, 300, True),
+                                          (45, 1, 64, 700, True), (45, 2, 256, 700, True),
+                                          (45, 4, 48, 700, True), (45, 16, 128, 700, False),
+                                          (45, 32, 32, 700, True), (45, 8, 192, 700, True),
+                                          (45, 4, 160, 700, True)])
+def test_f32_step_ragged_and_geometries(tbs, nq, H, D, nb, tail):
+    """fp32 queries through the step (in the fused kernel the eight CTAs of a
+    cluster each round a slice of the query tile and deliver it to all eight):
+    the rounded queries, the scores and the ids are bit-identical to the fp16
+    path on the same rounded queries, and the scores lie within the bound."""
+    block = 64
+    n_kv = nb * block - (13 if tail else 0)
+    k = 24
+    q32, kb = qi.random_case_f32(nq, H, D, nb, seed=nq * 131 + H * 7 + D, scale=0.5)
+    q16_buf = torch.empty(q32.shape, dtype=torch.float16, device="cuda")
+    q16_gpu, s_gpu, ids_gpu = tbs.qsa_select_step(dev(q32), dev(kb), n_kv, k, block, q16=q16_buf)
+    _, s_nq, ids_nq = tbs.qsa_select_step(dev(q32), dev(kb), n_kv, k, block)
+    q16 = orc.f32_to_f16(q32)
+    s_h, ids_h = tbs.qsa_score_select(dev(q16), dev(kb), n_kv, k, block)
+    torch.cuda.synchronize()
+    assert np.array_equal(q16_gpu.cpu().numpy().view(np.uint16), q16.view(np.uint16))
+    for s_x, i_x in ((s_gpu, ids_gpu), (s_nq, ids_nq)):
+        assert torch.equal(s_x.view(torch.int32), s_h.view(torch.int32))
+        assert torch.equal(i_x, ids_h)
+    s = s_gpu.cpu().numpy()
+    s_ref, S, B, tail_ref = orc.reference_scores(q16, kb, n_kv, block)
+    rep = orc.bound_report(s, s_ref, B)
+    assert rep["ok"], rep
+    if tail_ref is not None:
+        assert s[:, -1].view(np.uint32).tolist() == tail_ref.view(np.uint32).tolist()
+    assert np.array_equal(ids_gpu.cpu().numpy(), orc.select_topk(s, k))
+
+
 def test_select_step_host_matches_device(tbs):
     w = qi.WORKLOADS[2]
     q32, kb16 = qi.make_f32_inputs(w)[0], qi.make_inputs(w)[1]

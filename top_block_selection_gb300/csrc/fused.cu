@@ -29,9 +29,12 @@
 // into the selecting CTA's key array over distributed shared memory
 // (st.shared::cluster), so the select does not read the row back from
 // global memory; otherwise it reads the row after the barrier.
-// fp32 queries are loaded by all threads, rounded to fp16 (cvt.rn) and
-// written straight into the 128-byte-swizzled operand layout; fp16 queries
-// arrive by TMA. Every wait is bounded; a CTA that gives up still reaches the
+// fp32 queries are rounded to fp16 (cvt.rn) straight into the 128-byte-
+// swizzled operand layout. In DSMEM mode each CTA of the cluster rounds one
+// eighth of the group's rows and stores them (st.async) into all eight CTAs'
+// operand tiles, counted on each CTA's bar_q, so the cluster reads the fp32
+// tile from L2 once; otherwise every CTA converts the whole tile. fp16
+// queries arrive by TMA. Every wait is bounded; a CTA that gives up still reaches the
 // cluster barriers, so the cluster never hangs on them.
 #include <algorithm>
 #include <cstring>
@@ -66,6 +69,8 @@ struct FusedArgs {
   uint32_t sel_bytes;   // shared bytes of one select group (cand + sel, plus keys +
                         // hist in global mode)
   int32_t dsmem;        // 1: keys and first-digit histograms arrive over DSMEM
+  int32_t q_share;      // 1: each CTA converts 1/8 of the fp32 query tile and
+                        //    stores it into all eight CTAs' operand tiles (DSMEM)
   uint32_t row_bytes;   // DSMEM mode: bytes of one row's keys + histogram
   uint32_t rows_off;    // DSMEM mode: offset of the row regions in dynamic smem
   uint32_t* status;
@@ -110,6 +115,15 @@ __device__ __forceinline__ void st_async_u32(uint32_t addr, uint32_t v, uint32_t
                    addr),
                "r"(v), "r"(bar)
                : "memory");
+}
+
+// 16-byte remote store, signalled on the destination CTA's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, const uint4& v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          addr),
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
+      : "memory");
 }
 
 // Sends one score's key to keys[b] of the row's region in the CTA that
@@ -209,6 +223,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
       for (int r = 0; r < rows_here && q0 + rank + r * kCluster < a.nq; ++r) ++rows_valid;
       mbar_arrive_expect_tx(&bar_keys, static_cast<uint32_t>(rows_valid * a.nb) * 4u);
     }
+    // Shared query tile: the eight CTAs' slices arrive on bar_q.
+    if (a.q_share)
+      mbar_arrive_expect_tx(&bar_q, static_cast<uint32_t>(a.n_chunks * a.bn * kFRowBytes));
     if (n_local > 0) tma_prefetch_desc(&tm_kb);
     if (!kF32Q && need_q) tma_prefetch_desc(&tm_q);
     // Start this CTA's first operand tiles on their way from HBM to L2 while
@@ -216,7 +233,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
     for (int t = 0; t < 2 && t < n_local; ++t)
       for (int c = 0; c < a.n_chunks; ++c)
         tma_prefetch_l2_3d(&tm_kb, c * kFKAtom, (rank + t * kCluster) * kFTileM, kb_z);
-    if (need_q) {
+    if (a.q_share) {
+      const int rows_per = a.bn / kCluster, r0 = rank * rows_per;
+      const int rows = min(rows_per, qh_rows - r0);
+      if (rows > 0) {
+        const char* qp = reinterpret_cast<const char*>(q32b + static_cast<int64_t>(col0 + r0) * a.D);
+        bulk_prefetch_l2(qp, static_cast<uint32_t>(rows) * a.D * 4u);
+      }
+    } else if (need_q) {
       if (kF32Q) {
         const char* qp = reinterpret_cast<const char*>(q32b + static_cast<int64_t>(col0) * a.D);
         const uint32_t q_bytes = static_cast<uint32_t>(qh_rows) * a.D * 4u;
@@ -262,7 +286,55 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
     }
   }
   __syncwarp();
-  if (!producer_warp && kF32Q && need_q) {
+  // Work warps that already waited on the cluster start barrier (share mode).
+  bool cl_waited = false;
+  if (!producer_warp && kF32Q && a.q_share) {
+    // This CTA's slice of the query tile: rows [rank*bn/8, (rank+1)*bn/8),
+    // rounded to fp16 and stored as 16-byte swizzle units into every CTA of
+    // the cluster (its own included), counted on each CTA's bar_q. Rows past
+    // the last query and columns past D are sent as zeros, so every CTA
+    // receives the whole tile.
+    const int rows_per = a.bn / kCluster;
+    const int units_per_row = a.n_chunks * (kFKAtom / 8);
+    const int n_units = rows_per * units_per_row;
+    const uint32_t sq_local = smem_u32(sQ), bar_local = smem_u32(&bar_q);
+    auto load_unit = [&](int u, float4& v0, float4& v1) {
+      const int row = rank * rows_per + u / units_per_row;
+      const int i = (u % units_per_row) * 8;
+      v0 = make_float4(0.f, 0.f, 0.f, 0.f);
+      v1 = v0;
+      if (row < qh_rows && i < a.D) {
+        const float4* src =
+            reinterpret_cast<const float4*>(q32b + static_cast<int64_t>(col0 + row) * a.D + i);
+        v0 = __ldg(src);
+        v1 = __ldg(src + 1);
+      }
+    };
+    // The first unit's loads are in flight during the cluster wait.
+    float4 v0, v1;
+    if (tid < n_units) load_unit(tid, v0, v1);
+    cluster_wait_acquire();
+    cl_waited = true;
+    for (int u = tid; u < n_units; u += kWork) {
+      if (u != tid) load_unit(u, v0, v1);
+      const int row = rank * rows_per + u / units_per_row;
+      const int i = (u % units_per_row) * 8;
+      const __half2 h01 = __floats2half2_rn(v0.x, v0.y), h23 = __floats2half2_rn(v0.z, v0.w);
+      const __half2 h45 = __floats2half2_rn(v1.x, v1.y), h67 = __floats2half2_rn(v1.z, v1.w);
+      uint4 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&h01);
+      pk.y = *reinterpret_cast<const uint32_t*>(&h23);
+      pk.z = *reinterpret_cast<const uint32_t*>(&h45);
+      pk.w = *reinterpret_cast<const uint32_t*>(&h67);
+      if (q16outb != nullptr && row < qh_rows && i < a.D)
+        *reinterpret_cast<uint4*>(q16outb + static_cast<int64_t>(col0 + row) * a.D + i) = pk;
+      const uint32_t off = sw128_offset(a.bn, row, i);
+#pragma unroll
+      for (int dst = 0; dst < kCluster; ++dst)
+        st_async_v4(cluster_map(sq_local + off, static_cast<uint32_t>(dst)), pk,
+                    cluster_map(bar_local, static_cast<uint32_t>(dst)));
+    }
+  } else if (!producer_warp && kF32Q && need_q) {
     // fp32 queries -> fp16 (round to nearest even) -> swizzled operand tile,
     // by the kWork threads. Rows past the last query and columns past D are 0.
     const int f4_per_row = a.n_chunks * (kFKAtom / 4);
@@ -339,7 +411,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
     // ---------------------------------------------------- producer / MMA
     if (lane == 0 && n_local > 0) {
       const uint32_t idesc = idesc_f16_f32(kFTileM, a.bn);
-      bool ok = kF32Q ? true : mbar_wait_bounded(&bar_q, 0, a.timeout_ns);
+      bool ok = (kF32Q && !a.q_share) ? true : mbar_wait_bounded(&bar_q, 0, a.timeout_ns);
+      // Peers' st.async writes of the query tile, then the tensor core's reads.
+      if (a.q_share) fence_proxy_async_smem();
       for (int t = 0; t < n_local && ok; ++t) {
         const int s = t & 1;
         const uint32_t use = static_cast<uint32_t>(t >> 1);
@@ -387,10 +461,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
     // thread guarantee. Each warp waits just before its first remote store
     // (warp-uniform flag), which keeps the cluster's start skew off the
     // loads, the MMAs and the tail's dot products.
-    bool waited = !a.dsmem;
+    bool waited = !a.dsmem || cl_waited;
     // ------------------------------ tail block (warps 0..3 of the owner)
     if (tail_owner && warp < 4) {
-      if (!kF32Q && !mbar_wait_bounded(&bar_q, 0, a.timeout_ns)) {
+      if ((!kF32Q || a.q_share) && !mbar_wait_bounded(&bar_q, 0, a.timeout_ns)) {
         failed = 1;
         atomicOr(a.status, kErrScoreLoadTimeout);
       }
@@ -471,6 +545,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
     if (!waited) cluster_wait_acquire();
   }
 
+  // Share mode: every slice of the query tile has landed here before this
+  // CTA's shared memory is reused (select scratch) or released.
+  if (a.q_share && tid == 0 && !mbar_wait_bounded(&bar_q, 0, a.timeout_ns))
+    atomicOr(a.status, kErrScoreLoadTimeout);
   tc_fence_before_sync();
   __syncthreads();
   if (n_local > 0 && producer_warp) tmem_dealloc(tmem_base, a.tmem_cols);
@@ -678,6 +756,7 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
   const size_t row_bytes = (static_cast<size_t>(a.nb) * sizeof(uint32_t) + 15) & ~static_cast<size_t>(15);
   const size_t rows_off = (std::max(operand_bytes, core) + 1023) & ~static_cast<size_t>(1023);
   a.dsmem = (rows_off + rows_per_cta * row_bytes <= budget) ? 1 : 0;
+  a.q_share = (p.q32 != nullptr && a.dsmem && bn % kCluster == 0) ? 1 : 0;
   const size_t sel_bytes = a.dsmem ? core : core + static_cast<size_t>(a.nb) * sizeof(uint32_t);
   a.sel_bytes = static_cast<uint32_t>(sel_bytes);
   a.row_bytes = static_cast<uint32_t>(row_bytes);
