@@ -509,35 +509,32 @@ def run_split(torch, tbs, device, stream, peaks, peak_src, K, barrier):
     }
 
 
-E2E_STREAMS = 3
+E2E_STREAMS = int(os.environ.get("QSA_E2E_STREAMS", "6"))
 
 
 def run_e2e(torch, tbs, w, device, stream, K, W, barrier, with_q16):
-    """Same metric through qsa_select_step_host: each step copies its f32
-    queries and fp16 keys from pinned host memory, runs the step and copies
-    scores and ids back. Steps go round-robin to E2E_STREAMS streams, each
-    with its own device and host buffers, so one step's copies overlap
-    another's kernel (the copy engines and the SMs work at once); events on
-    `stream` bracket all K steps (every stream joins it at the end)."""
+    """Same metric through HostStep (qsa_select_step_host_packed): each step
+    copies its f32 queries and fp16 keys from one pinned host buffer (one
+    copy), runs the step and copies the selected ids back (the step's result;
+    the scores stay on the device). Steps go round-robin to E2E_STREAMS
+    streams, each with its own device buffers, so one step's copies overlap
+    another's kernel (the copy engines and the SMs work at once); two host
+    input sets alternate; events on `stream` bracket all K steps (every
+    stream joins it at the end)."""
     streams = [torch.cuda.Stream(device) for _ in range(E2E_STREAMS)]
+    steps = [tbs.HostStep(w.nq, w.H, w.D, w.n_kv, w.k, w.block, device=device, with_q16=with_q16,
+                          stream=streams[j]) for j in range(E2E_STREAMS)]
     inputs = []
     for v in range(2):
         q32, _ = qi.make_f32_inputs(w, variant=v)
         _, kb = qi.make_inputs(w, variant=v)
-        inputs.append((torch.from_numpy(q32).pin_memory(), torch.from_numpy(kb).pin_memory()))
-    outs = [(torch.empty((w.nq, w.nb), dtype=torch.float32).pin_memory(),
-             torch.empty((w.nq, w.k), dtype=torch.int32).pin_memory()) for _ in streams]
-    bufs = [(torch.empty((w.nq, w.H, w.D), dtype=torch.float32, device=device),
-             torch.empty((w.nq, w.H, w.D), dtype=torch.float16, device=device) if with_q16 else None,
-             torch.empty((w.nb, w.D), dtype=torch.float16, device=device),
-             torch.empty((w.nq, w.nb), dtype=torch.float32, device=device),
-             torch.empty((w.nq, w.k), dtype=torch.int32, device=device)) for _ in streams]
+        buf = steps[0].new_input()
+        steps[0].q32_view(buf).copy_(torch.from_numpy(q32))
+        steps[0].kb_view(buf).copy_(torch.from_numpy(kb))
+        inputs.append(buf)
 
     def one(i):
-        j = i % E2E_STREAMS
-        q32, kb = inputs[i % 2]
-        tbs.qsa_select_step_host(q32, kb, w.n_kv, w.k, w.block, outs[j][0], outs[j][1], bufs[j],
-                                 stream=streams[j])
+        steps[i % E2E_STREAMS](inputs[i % 2])
 
     def run(count):
         start = torch.cuda.Event()
@@ -558,10 +555,11 @@ def run_e2e(torch, tbs, w, device, stream, K, W, barrier, with_q16):
     med = statistics.median(ms)
     return {"value": aggregate_rate(world, units_per_step(w) * K, med), "unit": UNIT,
             "h2d_bytes_per_step": w.nq * w.H * w.D * 4 + w.nb * w.D * 2,
-            "d2h_bytes_per_step": w.nq * w.nb * 4 + w.nq * w.k * 4,
+            "d2h_bytes_per_step": w.nq * w.k * 4,
             "ms_per_step": med / K,
-            "api": f"qsa_select_step_host (pinned host buffers, eager calls over {E2E_STREAMS} "
-                   "streams)"}
+            "api": f"HostStep / qsa_select_step_host_packed (one pinned host buffer of f32 queries "
+                   f"and fp16 keys in, the selected ids out; eager calls over {E2E_STREAMS} "
+                   f"streams)"}
 
 
 # --------------------------------------------------------------- CPU oracle

@@ -205,17 +205,43 @@ qsa_status qsa_score_select_batched(const uint16_t* q, const uint16_t* kb, int64
 /*
  * qsa_select_step_host - qsa_select_step from HOST buffers: enqueues on
  * `stream` the copies q32_host -> q32_dev and kb_host -> kb_dev, the step,
- * and the copies scores_dev -> scores_host and ids_dev -> ids_host. Host
- * buffers should be page-locked for the copies to be asynchronous; they must
- * stay valid until the stream has finished the call's work (synchronize the
+ * and the copies scores_dev -> scores_host (unless scores_host is NULL: the
+ * scores then stay in scores_dev) and ids_dev -> ids_host. Host buffers
+ * should be page-locked for the copies to be asynchronous; they must stay
+ * valid until the stream has finished the call's work (synchronize the
  * stream before reading scores_host / ids_host). Device buffers are the
  * caller's, sized as for qsa_select_step (kb_dev: nb rows).
+ * Each host <-> device copy has a fixed cost of about 2 us on top of its
+ * bytes, and copies in one direction do not overlap one another:
+ * qsa_select_step_host_packed below makes one copy each way.
  */
 qsa_status qsa_select_step_host(const float* q32_host, const uint16_t* kb_host, int32_t nq,
                                 int32_t H, int32_t D, int64_t n_kv, int32_t block, int32_t k,
                                 float* scores_host, int32_t* ids_host, float* q32_dev,
                                 uint16_t* q16_dev, uint16_t* kb_dev, float* scores_dev,
                                 int32_t* ids_dev, qsa_stream_t stream);
+
+/*
+ * qsa_select_step_host_packed - qsa_select_step_host with each direction's
+ * buffers packed into one allocation, so that each direction is one copy
+ * (the pages' selection step fed from and read back to the host):
+ *   in_host / in_dev   q32 [nq,H,D] f32 at byte 0, then kb [nb,D] f16 at byte
+ *                      nq*H*D*4 (in_dev 16-byte aligned); in_host should be
+ *                      page-locked; in_dev is overwritten by the copy.
+ *   out_dev            scores [nq,nb] f32 at byte 0, then ids [nq,k] int32 at
+ *                      byte nq*nb*4.
+ *   out_host           with_scores != 0: scores then ids, as out_dev;
+ *                      with_scores == 0: ids [nq,k] only (the scores stay in
+ *                      out_dev).
+ *   q16_dev            optional fp16 copy of the converted queries, as for
+ *                      qsa_select_step.
+ * Enqueued on `stream`; host buffers must stay valid until the stream has
+ * finished the call's work. Errors as for qsa_select_step_host.
+ */
+qsa_status qsa_select_step_host_packed(const void* in_host, int32_t nq, int32_t H, int32_t D,
+                                       int64_t n_kv, int32_t block, int32_t k, void* out_host,
+                                       int32_t with_scores, void* in_dev, uint16_t* q16_dev,
+                                       void* out_dev, qsa_stream_t stream);
 
 /*
  * qsa_split_reduce - the flash-attention decode split reduce (a second

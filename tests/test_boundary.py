@@ -115,6 +115,21 @@ def test_convert_and_step_reject_bad_arguments_on_host(lib):
     assert step(A + 2, A) == MISALIGNED
 
 
+def test_packed_host_step_rejects_bad_arguments_on_host(lib):
+    A = 1 << 20
+    v = ctypes.c_void_p
+    pk = lambda nq, H, D, n_kv, k, in_h, out_h, in_d, out_d: lib.qsa_select_step_host_packed(
+        v(in_h), nq, H, D, n_kv, 64, k, v(out_h), 0, v(in_d), None, v(out_d), None)
+    assert pk(-1, 8, 128, 1000, 8, A, A, A, A) == INVALID
+    assert pk(4, 0, 128, 1000, 8, A, A, A, A) == INVALID
+    assert pk(4, 8, 120, 1000, 8, A, A, A, A) == GEOM          # D not a multiple of 16
+    assert pk(4, 8, 128, 1000, 8, A, A, 0, A) == INVALID       # no device input buffer
+    assert pk(4, 8, 128, 1000, 8, A, A, A + 2, A) == MISALIGNED
+    assert pk(4, 8, 128, 1000, 8, 0, A, A, A) == INVALID       # no host input buffer
+    assert pk(4, 8, 128, 1000, 8, A, 0, A, A) == INVALID       # no host output buffer
+    assert pk(0, 8, 128, 1000, 8, 0, 0, A, A) == OK            # nothing to do
+
+
 def test_batched_rejects_bad_arguments_on_host(lib):
     A = 1 << 20
     v = ctypes.c_void_p

@@ -392,6 +392,46 @@ def test_select_step_host_matches_device(tbs):
     assert np.array_equal(bufs[1].cpu().numpy().view(np.uint16), orc.f32_to_f16(q32).view(np.uint16))
 
 
+def test_select_step_host_packed_buffers(tbs):
+    """The packed host step (one copy each way) gives the same bits as the
+    device step, with the scores copied back or left on the device, and the
+    separate-buffer host step may leave the scores on the device too."""
+    w = qi.WORKLOADS[2]
+    q32, kb16 = qi.make_f32_inputs(w)[0], qi.make_inputs(w)[1]
+    _, s_d, i_d = tbs.qsa_select_step(dev(q32), dev(kb16), w.n_kv, w.k, w.block)
+    torch.cuda.synchronize()
+    for with_scores in (True, False):
+        step = tbs.HostStep(w.nq, w.H, w.D, w.n_kv, w.k, w.block, with_scores=with_scores,
+                            with_q16=True)
+        buf = step.new_input()
+        step.q32_view(buf).copy_(torch.from_numpy(q32))
+        step.kb_view(buf).copy_(torch.from_numpy(kb16))
+        step.ids_host.fill_(-7)
+        step(buf)
+        torch.cuda.synchronize()
+        assert np.array_equal(step.ids_host.numpy(), i_d.cpu().numpy())
+        assert torch.equal(step.scores_dev.view(torch.int32), s_d.view(torch.int32))
+        assert torch.equal(step.ids_dev, i_d)
+        assert np.array_equal(step.q16_dev.cpu().numpy().view(np.uint16),
+                              orc.f32_to_f16(q32).view(np.uint16))
+        if with_scores:
+            assert np.array_equal(step.scores_host.numpy().view(np.uint32),
+                                  s_d.cpu().numpy().view(np.uint32))
+        else:
+            assert step.scores_host is None
+    # qsa_select_step_host with scores_host None: ids back, scores on the device
+    ih = torch.full((w.nq, w.k), -7, dtype=torch.int32).pin_memory()
+    bufs = (torch.empty(q32.shape, dtype=torch.float32, device="cuda"), None,
+            torch.empty(kb16.shape, dtype=torch.float16, device="cuda"),
+            torch.zeros((w.nq, w.nb), dtype=torch.float32, device="cuda"),
+            torch.empty((w.nq, w.k), dtype=torch.int32, device="cuda"))
+    tbs.qsa_select_step_host(torch.from_numpy(q32).pin_memory(), torch.from_numpy(kb16).pin_memory(),
+                             w.n_kv, w.k, w.block, None, ih, bufs)
+    torch.cuda.synchronize()
+    assert np.array_equal(ih.numpy(), i_d.cpu().numpy())
+    assert torch.equal(bufs[3].view(torch.int32), s_d.view(torch.int32))
+
+
 def test_negative_control_on_gpu_scores(tbs):
     w = qi.WORKLOADS[0]
     q, kb = qi.make_inputs(w)

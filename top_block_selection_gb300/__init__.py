@@ -16,7 +16,8 @@ __all__ = [
     "QsaError", "load_library", "library_path", "qsa_abi_version", "qsa_status_str",
     "qsa_last_cuda_error", "qsa_arm",
     "qsa_num_blocks", "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select",
-    "qsa_select_step", "qsa_select_step_host", "qsa_device_status", "qsa_selftest_bounded_wait",
+    "qsa_select_step", "qsa_select_step_host", "qsa_select_step_host_packed", "HostStep",
+    "qsa_device_status", "qsa_selftest_bounded_wait",
     "qsa_select_step_batched", "qsa_score_select_batched", "qsa_select_step_launches",
     "qsa_split_reduce", "qsa_split_reduce_workspace_bytes", "EXPORTED_SYMBOLS",
 ]
@@ -28,8 +29,8 @@ _LIB = None
 EXPORTED_SYMBOLS = (
     "qsa_abi_version", "qsa_status_str", "qsa_last_cuda_error", "qsa_arm", "qsa_num_blocks",
     "qsa_f32_to_f16", "qsa_block_scores", "qsa_select", "qsa_score_select", "qsa_select_step",
-    "qsa_select_step_host", "qsa_device_status", "qsa_selftest_bounded_wait",
-    "qsa_select_step_batched", "qsa_score_select_batched", "qsa_select_step_launches",
+    "qsa_select_step_host", "qsa_select_step_host_packed", "qsa_device_status",
+    "qsa_selftest_bounded_wait", "qsa_select_step_batched", "qsa_score_select_batched", "qsa_select_step_launches",
     "qsa_split_reduce_workspace_bytes", "qsa_split_reduce", "qsa_split_reduce_static",
 )
 
@@ -75,6 +76,8 @@ def load_library():
         "qsa_select_step": (ctypes.c_int, [vp, vp, vp, i32, i32, i32, i64, i32, i32, vp, vp, vp]),
         "qsa_select_step_host": (ctypes.c_int, [vp, vp, i32, i32, i32, i64, i32, i32, vp, vp,
                                                 vp, vp, vp, vp, vp, vp]),
+        "qsa_select_step_host_packed": (ctypes.c_int, [vp, i32, i32, i32, i64, i32, i32, vp, i32,
+                                                       vp, vp, vp, vp]),
         "qsa_device_status": (ctypes.c_int, [ctypes.c_int, u32p, vp]),
         "qsa_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint64, vp]),
         "qsa_select_step_batched": (ctypes.c_int, [vp, vp, vp, i64, i32, i32, i32, i32, i64, i32,
@@ -268,11 +271,15 @@ def qsa_select_step_host(q32_host, kb_host, n_kv: int, k: int, block: int, score
                          dev_buffers, stream=None):
     """qsa_select_step from host (CPU, ideally pinned) tensors. dev_buffers =
     (q32_dev, q16_dev or None, kb_dev, scores_dev, ids_dev) CUDA tensors. Enqueued on
-    `stream` (default: current stream); synchronize before reading outputs."""
+    `stream` (default: current stream); synchronize before reading outputs.
+    scores_host None leaves the scores in scores_dev. Buffers from
+    host_step_buffers() are packed, so each direction is one copy."""
     torch = _torch()
     q32_dev, q16_dev, kb_dev, scores_dev, ids_dev = dev_buffers
     for t, name in ((q32_host, "q32_host"), (kb_host, "kb_host"), (scores_host, "scores_host"),
                     (ids_host, "ids_host")):
+        if t is None and name == "scores_host":
+            continue
         if t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous host tensor")
     nq, H, D = q32_host.shape
@@ -281,10 +288,124 @@ def qsa_select_step_host(q32_host, kb_host, n_kv: int, k: int, block: int, score
     lib = load_library()
     with torch.cuda.device(q32_dev.device):
         _check(lib.qsa_select_step_host(
-            _ptr(q32_host), _ptr(kb_host), nq, H, D, n_kv, block, k, _ptr(scores_host),
+            _ptr(q32_host), _ptr(kb_host), nq, H, D, n_kv, block, k,
+            _ptr(scores_host) if scores_host is not None else None,
             _ptr(ids_host), _ptr(q32_dev), _ptr(q16_dev) if q16_dev is not None else None,
             _ptr(kb_dev), _ptr(scores_dev),
             _ptr(ids_dev), ctypes.c_void_p(stream.cuda_stream)), "qsa_select_step_host")
+
+
+def qsa_select_step_host_packed(in_host, nq: int, H: int, D: int, n_kv: int, k: int, block: int,
+                                out_host, in_dev, out_dev, q16_dev=None, with_scores: bool = False,
+                                stream=None):
+    """The step from packed byte buffers (uint8 tensors): in_host / in_dev =
+    q32 [nq,H,D] f32 then kb [nb,D] f16; out_dev = scores [nq,nb] f32 then
+    ids [nq,k] int32; out_host = the same (with_scores) or ids only. One copy
+    each way, enqueued on `stream` (default: current stream)."""
+    torch = _torch()
+    nb = qsa_num_blocks(n_kv, block)
+    if nb < 0:
+        raise ValueError("n_kv >= 0 and block >= 1 required")
+    in_bytes = nq * H * D * 4 + nb * D * 2
+    out_dev_bytes = nq * nb * 4 + nq * k * 4
+    out_host_bytes = out_dev_bytes if with_scores else nq * k * 4
+    for t, cuda, size, name in ((in_host, False, in_bytes, "in_host"), (in_dev, True, in_bytes, "in_dev"),
+                                (out_dev, True, out_dev_bytes, "out_dev"),
+                                (out_host, False, out_host_bytes, "out_host")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.uint8 or t.is_cuda != cuda \
+                or not t.is_contiguous() or t.numel() < size:
+            raise ValueError(f"{name} must be a contiguous {'CUDA' if cuda else 'host'} uint8 tensor "
+                             f"of at least {size} bytes")
+    if q16_dev is not None:
+        _need(q16_dev, torch.float16, 3, "q16_dev")
+    if stream is None:
+        stream = torch.cuda.current_stream(in_dev.device)
+    lib = load_library()
+    with torch.cuda.device(in_dev.device):
+        _check(lib.qsa_select_step_host_packed(
+            _ptr(in_host), nq, H, D, n_kv, block, k, _ptr(out_host), 1 if with_scores else 0,
+            _ptr(in_dev), _ptr(q16_dev) if q16_dev is not None else None, _ptr(out_dev),
+            ctypes.c_void_p(stream.cuda_stream)), "qsa_select_step_host_packed")
+
+
+class HostStep:
+    """A selection step fed from and read back to the host, bound to fixed
+    sizes, its own packed device buffers and a stream (a serving loop's
+    per-step state): one copy in (queries then keys), the step, one copy out
+    (the ids, or scores then ids). Checks and pointer marshalling of the fixed
+    parts are done once; a call marshals only the input buffer.
+
+        step = HostStep(nq, H, D, n_kv, k, block)
+        buf = step.new_input()            # pinned; fill step.q32_view(buf), step.kb_view(buf)
+        step(buf)                         # enqueue; then synchronize the stream
+        step.ids_host / step.scores_host  # results (scores_host: with_scores=True)
+    """
+
+    def __init__(self, nq: int, H: int, D: int, n_kv: int, k: int, block: int = 64, device=None,
+                 with_scores: bool = False, with_q16: bool = False, stream=None):
+        torch = _torch()
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
+            else torch.device(device)
+        nb = qsa_num_blocks(n_kv, block)
+        if nb < 0 or nq < 0 or H < 1 or D < 1 or k < 1:
+            raise ValueError("bad step sizes")
+        self.nq, self.H, self.D, self.nb, self.k = nq, H, D, nb, k
+        self.n_kv, self.block, self.with_scores = n_kv, block, with_scores
+        self._qb, self._kbb = nq * H * D * 4, nb * D * 2
+        self._sb, self._ib = nq * nb * 4, nq * k * 4
+        self.in_dev = torch.empty(self._qb + self._kbb, dtype=torch.uint8, device=self.device)
+        self.out_dev = torch.empty(self._sb + self._ib, dtype=torch.uint8, device=self.device)
+        self.q16_dev = (torch.empty((nq, H, D), dtype=torch.float16, device=self.device)
+                        if with_q16 else None)
+        self.out_host = torch.empty(self._sb + self._ib if with_scores else self._ib,
+                                    dtype=torch.uint8).pin_memory()
+        self.stream = torch.cuda.current_stream(self.device) if stream is None else stream
+        self._fn = load_library().qsa_select_step_host_packed
+        self._fixed_tail = (_ptr(self.out_host), 1 if with_scores else 0, _ptr(self.in_dev),
+                            _ptr(self.q16_dev) if self.q16_dev is not None else None,
+                            _ptr(self.out_dev), ctypes.c_void_p(self.stream.cuda_stream))
+        self._dims = (nq, H, D, n_kv, block, k)
+
+    def new_input(self):
+        """A pinned input buffer for this step's sizes."""
+        return _torch().empty(self._qb + self._kbb, dtype=_torch().uint8).pin_memory()
+
+    def q32_view(self, buf):
+        return buf[:self._qb].view(_torch().float32).view(self.nq, self.H, self.D)
+
+    def kb_view(self, buf):
+        return buf[self._qb:self._qb + self._kbb].view(_torch().float16).view(self.nb, self.D)
+
+    @property
+    def ids_host(self):
+        off = self._sb if self.with_scores else 0
+        return self.out_host[off:off + self._ib].view(_torch().int32).view(self.nq, self.k)
+
+    @property
+    def scores_host(self):
+        if not self.with_scores:
+            return None
+        return self.out_host[:self._sb].view(_torch().float32).view(self.nq, self.nb)
+
+    @property
+    def scores_dev(self):
+        return self.out_dev[:self._sb].view(_torch().float32).view(self.nq, self.nb)
+
+    @property
+    def ids_dev(self):
+        return self.out_dev[self._sb:self._sb + self._ib].view(_torch().int32).view(self.nq, self.k)
+
+    def __call__(self, in_host):
+        torch = _torch()
+        if in_host.dtype != torch.uint8 or in_host.is_cuda or in_host.numel() < self._qb + self._kbb \
+                or not in_host.is_contiguous():
+            raise ValueError("in_host must be a contiguous host uint8 buffer from new_input()")
+        if torch.cuda.current_device() != self.device.index:
+            with torch.cuda.device(self.device):
+                return self(in_host)
+        nq, H, D, n_kv, block, k = self._dims
+        _check(self._fn(_ptr(in_host), nq, H, D, n_kv, block, k, *self._fixed_tail),
+               "qsa_select_step_host_packed")
 
 
 def qsa_device_status(clear: bool = True, device=None):

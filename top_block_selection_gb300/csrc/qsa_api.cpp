@@ -278,7 +278,7 @@ qsa_status qsa_select_step_host(const float* q32_host, const uint16_t* kb_host, 
   if ((st = check_select(scores_dev, nq, g.nb, k, ids_dev)) != QSA_OK) return st;
   if (nq == 0) return QSA_OK;
   if (!q32_host || !ids_host || !q32_dev || !ids_dev) return QSA_ERR_INVALID_ARG;
-  if (g.nb > 0 && (!kb_host || !scores_host)) return QSA_ERR_INVALID_ARG;
+  if (g.nb > 0 && !kb_host) return QSA_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
   cudaStream_t s = as_cuda(stream);
@@ -294,10 +294,50 @@ qsa_status qsa_select_step_host(const float* q32_host, const uint16_t* kb_host, 
   st = qsa_select_step(q32_dev, q16_dev, kb_dev, nq, H, D, n_kv, block, k, scores_dev, ids_dev,
                        stream);
   if (st != QSA_OK) return st;
-  if (s_bytes &&
+  if (s_bytes && scores_host &&
       cudaMemcpyAsync(scores_host, scores_dev, s_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return cuda_fail(cudaGetLastError());
   if (cudaMemcpyAsync(ids_host, ids_dev, id_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return cuda_fail(cudaGetLastError());
+  return QSA_OK;
+}
+
+qsa_status qsa_select_step_host_packed(const void* in_host, int32_t nq, int32_t H, int32_t D,
+                                       int64_t n_kv, int32_t block, int32_t k, void* out_host,
+                                       int32_t with_scores, void* in_dev, uint16_t* q16_dev,
+                                       void* out_dev, qsa_stream_t stream) {
+  if (nq < 0 || H < 1 || D < 1) return QSA_ERR_INVALID_ARG;
+  const int64_t nb = qsa_num_blocks(n_kv, block);
+  if (nb < 0) return QSA_ERR_INVALID_ARG;
+  const size_t q_bytes = static_cast<size_t>(nq) * H * D * sizeof(float);
+  const size_t kb_bytes = static_cast<size_t>(nb) * D * sizeof(uint16_t);
+  const size_t s_bytes = static_cast<size_t>(nq) * nb * sizeof(float);
+  const size_t id_bytes = static_cast<size_t>(nq) * (k > 0 ? k : 0) * sizeof(int32_t);
+  char* in_d = static_cast<char*>(in_dev);
+  char* out_d = static_cast<char*>(out_dev);
+  float* q32_dev = reinterpret_cast<float*>(in_d);
+  uint16_t* kb_dev = in_d ? reinterpret_cast<uint16_t*>(in_d + q_bytes) : nullptr;
+  float* scores_dev = reinterpret_cast<float*>(out_d);
+  int32_t* ids_dev = out_d ? reinterpret_cast<int32_t*>(out_d + s_bytes) : nullptr;
+  Geometry g;
+  qsa_status st = check_scores(reinterpret_cast<const uint16_t*>(q32_dev), kb_dev, nq, H, D, n_kv,
+                               block, scores_dev, &g);
+  if (st != QSA_OK) return st;
+  if ((st = check_select(scores_dev, nq, g.nb, k, ids_dev)) != QSA_OK) return st;
+  if (nq == 0) return QSA_OK;
+  if (!in_host || !out_host || !in_dev || !out_dev) return QSA_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  cudaStream_t s = as_cuda(stream);
+  // One copy in (queries then keys), one copy out (scores then ids, or ids).
+  if (cudaMemcpyAsync(in_dev, in_host, q_bytes + kb_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return cuda_fail(cudaGetLastError());
+  st = qsa_select_step(q32_dev, q16_dev, kb_dev, nq, H, D, n_kv, block, k, scores_dev, ids_dev,
+                       stream);
+  if (st != QSA_OK) return st;
+  const void* src = with_scores ? static_cast<const void*>(scores_dev) : static_cast<const void*>(ids_dev);
+  const size_t out_bytes = with_scores ? s_bytes + id_bytes : id_bytes;
+  if (cudaMemcpyAsync(out_host, src, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return cuda_fail(cudaGetLastError());
   return QSA_OK;
 }
