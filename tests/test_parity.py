@@ -250,6 +250,31 @@ def test_batched_step_equals_single_steps(tbs, w, shared_kb):
     assert np.array_equal(ib[1].cpu().numpy(), orc.select_topk(s1, w.k))
 
 
+@pytest.mark.parametrize("nq,nb,n_batches", [(256, 2048, 3), (64, 3000, 6)])
+def test_batched_lean_form(tbs, nq, nb, n_batches):
+    """Launches of several waves take the lean form (one Kb stage, capped
+    registers); its bits equal the single-batch launches' (the regular form),
+    with two tiles per CTA and with three (the stage refilled between tiles)."""
+    H, D, k = 8, 128, 64
+    n_kv = nb * 64 - 5
+    cases = [qi.random_case_f32(nq, H, D, nb, seed=7000 + 31 * b + nb, scale=0.25) for b in range(n_batches)]
+    q32 = np.stack([c[0] for c in cases])
+    kbs = np.stack([c[1] for c in cases])
+    _, sb, ib = tbs.qsa_select_step_batched(dev(q32), dev(kbs), n_kv, k, 64)
+    torch.cuda.synchronize()
+    for b in range(n_batches):
+        _, ss, is_ = tbs.qsa_select_step(dev(q32[b]), dev(kbs[b]), n_kv, k, 64)
+        torch.cuda.synchronize()
+        assert torch.equal(sb[b].view(torch.int32), ss.view(torch.int32)), b
+        assert torch.equal(ib[b], is_), b
+    q16 = orc.f32_to_f16(q32[-1])
+    s_ref, S, B_, tail = orc.reference_scores(q16, kbs[-1], n_kv, 64)
+    s_last = sb[-1].cpu().numpy()
+    assert orc.bound_report(s_last, s_ref, B_)["ok"]
+    assert s_last[:, -1].view(np.uint32).tolist() == tail.view(np.uint32).tolist()
+    assert np.array_equal(ib[-1].cpu().numpy(), orc.select_topk(s_last, k))
+
+
 def test_batched_score_select_fp16(tbs):
     w = qi.WORKLOADS[1]
     B = 4

@@ -65,6 +65,7 @@ struct FusedArgs {
   int64_t q_batch_elems;     // nq * H * D: q32 / q16 / q16out elements per batch
   int64_t kb_batch_stride;   // kb elements between batches; 0 = one kb shared by all
   int32_t bn, qg, m_tiles, n_chunks, k_steps;
+  int32_t kb_stages;    // shared-memory stages for Kb tiles (2; 1 in the lean form)
   uint32_t tmem_cols;
   uint32_t sel_bytes;   // shared bytes of one select group (cand + sel, plus keys +
                         // hist in global mode)
@@ -158,8 +159,10 @@ __device__ __forceinline__ uint32_t sw128_offset(int rows, int row, int i) {
                                ((unit ^ (row & 7)) << 4) + ((i & 7) << 1));
 }
 
-template <int H, bool kF32Q>
-__global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
+// kLean: at most 72 registers per thread (with one Kb stage, three CTAs fit
+// an SM), for launches of many waves where CTAs overlap one another.
+template <int H, bool kF32Q, bool kLean>
+__global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(kLean ? 72 : 96)
     fused_step_kernel(const __grid_constant__ CUtensorMap tm_kb,
                       const __grid_constant__ CUtensorMap tm_q, const FusedArgs a) {
   static_assert(32 % H == 0, "a 32-column TMEM load must hold whole queries");
@@ -174,7 +177,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint8_t* sQ = smem;                                             // n_chunks x bn rows x 128 B
-  uint8_t* sKB = sQ + a.n_chunks * a.bn * kFRowBytes;              // 2 stages
+  uint8_t* sKB = sQ + a.n_chunks * a.bn * kFRowBytes;              // kb_stages stages
   const int stage_bytes = a.n_chunks * kFTileM * kFRowBytes;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -277,7 +280,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
       for (int c = 0; c < a.n_chunks; ++c)
         tma_load_2d(sQ + c * a.bn * kFRowBytes, &tm_q, c * kFKAtom, q_row0 + col0, &bar_q);
     }
-    for (int t = 0; t < 2 && t < n_local; ++t) {
+    for (int t = 0; t < a.kb_stages && t < n_local; ++t) {
       const int m = rank + t * kCluster;
       mbar_arrive_expect_tx(&bar_full[t], static_cast<uint32_t>(stage_bytes));
       for (int c = 0; c < a.n_chunks; ++c)
@@ -415,16 +418,18 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
       // Peers' st.async writes of the query tile, then the tensor core's reads.
       if (a.q_share) fence_proxy_async_smem();
       for (int t = 0; t < n_local && ok; ++t) {
-        const int s = t & 1;
+        const int s = t & 1;  // accumulator
         const uint32_t use = static_cast<uint32_t>(t >> 1);
-        if (!mbar_wait_bounded(&bar_full[s], use & 1u, a.timeout_ns)) { ok = false; break; }
+        const int ks = t % a.kb_stages;  // Kb stage
+        const uint32_t kuse = static_cast<uint32_t>(t / a.kb_stages);
+        if (!mbar_wait_bounded(&bar_full[ks], kuse & 1u, a.timeout_ns)) { ok = false; break; }
         if (t >= 2 && !mbar_wait_bounded(&bar_acc_empty[s], (use - 1) & 1u, a.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(s * a.bn);
-        const uint32_t a_base = smem_u32(sKB + s * stage_bytes);
+        const uint32_t a_base = smem_u32(sKB + ks * stage_bytes);
         const uint32_t b_base = smem_u32(sQ);
         for (int step = 0; step < a.k_steps; ++step) {
           const int c = step >> 2, kk = step & 3;
@@ -433,14 +438,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
                      step > 0 ? 1u : 0u);
         }
         mma_commit(&bar_acc_full[s]);
-        mma_commit(&bar_empty[s]);
-        if (t + 2 < n_local) {
-          if (!mbar_wait_bounded(&bar_empty[s], use & 1u, a.timeout_ns)) { ok = false; break; }
-          const int m = rank + (t + 2) * kCluster;
-          mbar_arrive_expect_tx(&bar_full[s], static_cast<uint32_t>(stage_bytes));
+        mma_commit(&bar_empty[ks]);
+        if (t + a.kb_stages < n_local) {
+          if (!mbar_wait_bounded(&bar_empty[ks], kuse & 1u, a.timeout_ns)) { ok = false; break; }
+          const int m = rank + (t + a.kb_stages) * kCluster;
+          mbar_arrive_expect_tx(&bar_full[ks], static_cast<uint32_t>(stage_bytes));
           for (int c = 0; c < a.n_chunks; ++c)
-            tma_load_3d(sKB + s * stage_bytes + c * kFTileM * kFRowBytes, &tm_kb, c * kFKAtom,
-                        m * kFTileM, kb_z, &bar_full[s]);
+            tma_load_3d(sKB + ks * stage_bytes + c * kFTileM * kFRowBytes, &tm_kb, c * kFKAtom,
+                        m * kFTileM, kb_z, &bar_full[ks]);
         }
       }
       if (!ok) {
@@ -450,7 +455,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
         // wait out its own bound, then drain loads still in flight.
         mma_commit(&bar_acc_full[0]);
         mma_commit(&bar_acc_full[1]);
-        for (int s = 0; s < 2 && s < n_local; ++s) mbar_wait_bounded(&bar_full[s], 0, a.timeout_ns);
+        for (int s = 0; s < a.kb_stages && s < n_local; ++s) mbar_wait_bounded(&bar_full[s], 0, a.timeout_ns);
       }
     }
     __syncwarp();
@@ -628,18 +633,19 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(96)
 namespace {
 
 template <int H, bool F>
-const void* fused_ptr() {
-  return reinterpret_cast<const void*>(&fused_step_kernel<H, F>);
+const void* fused_ptr(bool lean) {
+  return lean ? reinterpret_cast<const void*>(&fused_step_kernel<H, F, true>)
+              : reinterpret_cast<const void*>(&fused_step_kernel<H, F, false>);
 }
 
-const void* fused_kernel_for(int H, bool f32q) {
+const void* fused_kernel_for(int H, bool f32q, bool lean) {
   switch (H) {
-    case 1: return f32q ? fused_ptr<1, true>() : fused_ptr<1, false>();
-    case 2: return f32q ? fused_ptr<2, true>() : fused_ptr<2, false>();
-    case 4: return f32q ? fused_ptr<4, true>() : fused_ptr<4, false>();
-    case 8: return f32q ? fused_ptr<8, true>() : fused_ptr<8, false>();
-    case 16: return f32q ? fused_ptr<16, true>() : fused_ptr<16, false>();
-    case 32: return f32q ? fused_ptr<32, true>() : fused_ptr<32, false>();
+    case 1: return f32q ? fused_ptr<1, true>(lean) : fused_ptr<1, false>(lean);
+    case 2: return f32q ? fused_ptr<2, true>(lean) : fused_ptr<2, false>(lean);
+    case 4: return f32q ? fused_ptr<4, true>(lean) : fused_ptr<4, false>(lean);
+    case 8: return f32q ? fused_ptr<8, true>(lean) : fused_ptr<8, false>(lean);
+    case 16: return f32q ? fused_ptr<16, true>(lean) : fused_ptr<16, false>(lean);
+    case 32: return f32q ? fused_ptr<32, true>(lean) : fused_ptr<32, false>(lean);
     default: return nullptr;
   }
 }
@@ -677,22 +683,23 @@ int g_fused_static_smem = 0;
 
 cudaError_t init_fused_kernels(const DeviceInfo& dev) {
   for (int H : {1, 2, 4, 8, 16, 32})
-    for (bool f : {false, true}) {
-      cudaFuncAttributes fa;
-      cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel_for(H, f));
-      if (e != cudaSuccess) return e;
-      g_fused_static_smem = std::max(g_fused_static_smem, static_cast<int>(fa.sharedSizeBytes));
-      e = cudaFuncSetAttribute(fused_kernel_for(H, f), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dev.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
-      if (e != cudaSuccess) return e;
-      // Always the largest shared-memory carveout: two CTAs of a cluster per
-      // SM need it, and a smaller carveout chosen from one launch's request
-      // left room for one cluster CTA per SM (half the clusters resident).
-      e = cudaFuncSetAttribute(fused_kernel_for(H, f),
-                               cudaFuncAttributePreferredSharedMemoryCarveout,
-                               cudaSharedmemCarveoutMaxShared);
-      if (e != cudaSuccess) return e;
-    }
+    for (bool f : {false, true})
+      for (bool lean : {false, true}) {
+        const void* fn = fused_kernel_for(H, f, lean);
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+        if (e != cudaSuccess) return e;
+        g_fused_static_smem = std::max(g_fused_static_smem, static_cast<int>(fa.sharedSizeBytes));
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 dev.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
+        if (e != cudaSuccess) return e;
+        // Always the largest shared-memory carveout: two CTAs of a cluster per
+        // SM need it, and a smaller carveout chosen from one launch's request
+        // left room for one cluster CTA per SM (half the clusters resident).
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+      }
   return cudaSuccess;
 }
 
@@ -742,7 +749,13 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
   a.status = dev.status_word;
   a.timeout_ns = kWaitTimeoutNs;
   const int rows_per_cta = (qg + kCluster - 1) / kCluster;
-  const size_t operand_bytes = static_cast<size_t>(a.n_chunks) * (bn + 2 * kFTileM) * kFRowBytes;
+  // Lean form for launches of several waves (CTAs overlap one another's
+  // phases): one Kb stage and at most 72 registers, so three CTAs fit an SM;
+  // only while three CTAs' TMEM columns fit the SM's 512.
+  const bool lean = blocks > 2LL * dev.sm_count && 3u * (2u * static_cast<uint32_t>(bn)) <= 512u;
+  a.kb_stages = lean ? 1 : 2;
+  const size_t operand_bytes =
+      static_cast<size_t>(a.n_chunks) * (bn + a.kb_stages * kFTileM) * kFRowBytes;
   const size_t budget = static_cast<size_t>(dev.max_smem_optin) - g_fused_static_smem - 1024;
   // Select scratch in the operand region after the epilogue: hist, excl,
   // cand, sel, sel_bin, and (global mode, long rows) the row's staged keys
@@ -779,7 +792,7 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
       !encode_f16_2d(&tm_q, p.q16, p.D, static_cast<uint64_t>(p.n_batches) * p.nq * p.H, kFKAtom, bn))
     return cudaErrorInvalidValue;
   const bool f32q = p.q32 != nullptr;
-  const void* fn = fused_kernel_for(p.H, f32q);
+  const void* fn = fused_kernel_for(p.H, f32q, lean);
   if (fn == nullptr) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
