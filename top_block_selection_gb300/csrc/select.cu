@@ -2,8 +2,10 @@
 // part 1 and pull request 856, "Arithmetic contract and parity": the top-k
 // over the block scores, here with a block-index tie-break).
 //
-// A CTA of kSelThreads threads selects kSelRowsPerCta rows, kSelG warps per
-// row (see select_row_g in select_row.cuh for the algorithm): the row's keys
+// Rows of up to 4096 blocks: one CTA of 8 warps per row, the row's keys in
+// registers, the window select of the fused kernel (select_row_window, with
+// select_row_regs behind it). Longer rows: a CTA of kSelThreads threads
+// selects several rows, kSelG warps per row (select_row_g): the row's keys
 // are staged in shared memory, the first 11-bit radix digit finds the
 // boundary bin, the boundary bin's keys are compacted and refined, and the
 // winners are rank-sorted.
@@ -59,7 +61,47 @@ __global__ void __launch_bounds__(kSelThreads)
   select_row_g<kSelG>(keys, nb, k, ids + row * k, hist, cand, sel, sh[g], gtid, 1 + g);
 }
 
+constexpr int kWinThreads = 256;
+
+// Shared bytes of the window select: hist, excl, cand, sel (k), sel_bin (k
+// rounded up to 4).
+inline size_t select_window_bytes(int32_t k) {
+  return 2 * kSelHistBins * sizeof(uint32_t) + (static_cast<size_t>(kSelBinMax) + k) * sizeof(uint64_t) +
+         ((static_cast<size_t>(k) + 3) & ~static_cast<size_t>(3)) * sizeof(uint32_t);
+}
+
+template <int R>
+__global__ void __launch_bounds__(kWinThreads)
+    select_window_kernel(const float* __restrict__ scores, int32_t nb, int32_t k,
+                         int32_t* __restrict__ ids) {
+  extern __shared__ __align__(16) uint8_t sm_raw[];
+  __shared__ SelectShared sh;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sm_raw);
+  uint32_t* excl = hist + kSelHistBins;
+  uint64_t* cand = reinterpret_cast<uint64_t*>(excl + kSelHistBins);
+  uint64_t* sel = cand + kSelBinMax;
+  uint32_t* sel_bin = reinterpret_cast<uint32_t*>(sel + k);
+  const int tid = threadIdx.x;
+  const int64_t row = blockIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();  // the scores may come from the previous kernel on the stream
+  uint32_t key[R];
+  load_keys_regs_global<kWinThreads, R>(scores + row * nb, nb, key, hist, tid);
+  int32_t* out = ids + row * k;
+  if (!select_row_window<kWinThreads, R>(key, nb, k, out, hist, excl, cand, sel, sel_bin, sh, tid, 1)) {
+    build_first_digit_hist<kWinThreads, R>(key, nb, hist, tid, 1);
+    select_row_regs<kWinThreads, R>(key, nb, k, out, hist, cand, sel, sh, tid, 1);
+  }
+}
+
 cudaError_t init_select_kernels(const DeviceInfo& dev) {
+  for (const void* fn : {reinterpret_cast<const void*>(&select_window_kernel<8>),
+                         reinterpret_cast<const void*>(&select_window_kernel<12>),
+                         reinterpret_cast<const void*>(&select_window_kernel<16>)}) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(select_window_bytes(1024)));
+    if (e != cudaSuccess) return e;
+  }
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&select_kernel));
   if (e != cudaSuccess) return e;
@@ -71,6 +113,15 @@ cudaError_t init_select_kernels(const DeviceInfo& dev) {
 cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k, int32_t* ids,
                           const DeviceInfo& dev, cudaStream_t stream) {
   if (nq <= 0) return cudaSuccess;
+  if (nb >= 1 && nb <= 16 * kWinThreads && k <= 1024) {
+    const size_t smem = select_window_bytes(k);
+    const dim3 grid(static_cast<unsigned>(nq)), block(kWinThreads);
+    if (nb <= 8 * kWinThreads)
+      return launch_pdl(select_window_kernel<8>, grid, block, smem, stream, scores, nb, k, ids);
+    if (nb <= 12 * kWinThreads)
+      return launch_pdl(select_window_kernel<12>, grid, block, smem, stream, scores, nb, k, ids);
+    return launch_pdl(select_window_kernel<16>, grid, block, smem, stream, scores, nb, k, ids);
+  }
   const size_t per = select_group_bytes(nb, k);
   const size_t room = static_cast<size_t>(dev.max_smem_optin) - sizeof(GroupShared) * kSelMaxGroups;
   int groups = kSelMaxGroups;
