@@ -72,6 +72,10 @@ def parse_args():
     p.add_argument("--no-split", action="store_true",
                    help="skip the split-reduce (second workload) measurement")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="skip the per-workload measurements (per_config)")
+    p.add_argument("--per-config-cpu-seconds", type=float, default=1.5,
+                   help="CPU oracle budget per workload in per_config")
     return p.parse_args()
 
 
@@ -184,19 +188,31 @@ class Sets:
     """Rotating device buffer sets for one workload, stored as contiguous
     [n, ...] tensors so that a slice of consecutive sets is itself a batch."""
 
-    def __init__(self, torch, tbs, w, device, min_bytes, rank=0):
-        per = (w.nq * w.H * w.D * (4 + 2) + w.nb * w.D * 2 + w.nq * w.nb * 4 + w.nq * w.k * 4)
-        n = max(2, math.ceil(min_bytes / per))
-        self.n = ((n + 7) // 8) * 8  # whole groups of 8 for the batched launch
+    @staticmethod
+    def bytes_per_set(w):
+        return w.nq * w.H * w.D * (4 + 2) + w.nb * w.D * 2 + w.nq * w.nb * 4 + w.nq * w.k * 4
+
+    def __init__(self, torch, tbs, w, device, min_bytes, rank=0, max_distinct=None, min_sets=2):
+        per = Sets.bytes_per_set(w)
+        n = max(min_sets, math.ceil(min_bytes / per))
+        self.n = ((n + 7) // 8) * 8 if n > 8 else n  # whole groups of 8 for the batched launch
         self.per_set_bytes = per
         self.variants = rank_variants(rank, self.n)
         self.q32 = torch.empty((self.n, w.nq, w.H, w.D), dtype=torch.float32, device=device)
         self.kb = torch.empty((self.n, w.nb, w.D), dtype=torch.float16, device=device)
-        for v, var in enumerate(self.variants):
+        # Small workloads need thousands of sets to exceed L2: draw up to
+        # max_distinct seeded sets and fill the rest with copies of them (the
+        # copies are distinct buffers, so every step still reads from HBM).
+        distinct = self.n if max_distinct is None else min(self.n, max_distinct)
+        for v, var in enumerate(list(self.variants)[:distinct]):
             q32, _ = qi.make_f32_inputs(w, variant=var)
             _, kb = qi.make_inputs(w, variant=var)
             self.q32[v].copy_(torch.from_numpy(q32))
             self.kb[v].copy_(torch.from_numpy(kb))
+        for v0 in range(distinct, self.n, distinct):
+            m = min(distinct, self.n - v0)
+            self.q32[v0:v0 + m].copy_(self.q32[:m])
+            self.kb[v0:v0 + m].copy_(self.kb[:m])
         self.q16 = torch.empty((self.n, w.nq, w.H, w.D), dtype=torch.float16, device=device)
         self.scores = torch.empty((self.n, w.nq, w.nb), dtype=torch.float32, device=device)
         self.ids = torch.empty((self.n, w.nq, w.k), dtype=torch.int32, device=device)
@@ -216,15 +232,40 @@ def graph_of(torch, stream, fn, count):
     return g
 
 
-def time_region(torch, stream, replay, reps_min, seconds, barrier=None):
+def rotating_replay(torch, stream, fn, count, n_sets):
+    """Graphs of exactly `count` calls each, graph j calling fn(j * count + i)
+    for i < count, enough of them that together they touch all n_sets input
+    sets; the returned replay() runs the next graph in turn. With n_sets
+    sets larger than twice L2 in total, a set is touched again only after
+    every other set has been, so each replay reads its inputs from HBM
+    whatever `count` is."""
+    n_graphs = max(1, -(-n_sets // count))
+    graphs = [graph_of(torch, stream, lambda i, j=j: fn(j * count + i), count)
+              for j in range(n_graphs)]
+    state = {"next": 0}
+
+    def replay():
+        g = graphs[state["next"]]
+        state["next"] = (state["next"] + 1) % n_graphs
+        with torch.cuda.stream(stream):
+            g.replay()
+    for _ in range(n_graphs):  # upload + one untimed replay of each graph
+        replay()
+    return replay
+
+
+def time_region(torch, stream, replay, reps_min, seconds, barrier=None, pre=None):
     """Time replay() (exactly K steps) with CUDA events on `stream`, repeated
-    until `seconds` have passed (at least reps_min times). Returns the list of
-    elapsed milliseconds, each the max over ranks."""
+    until `seconds` have passed (at least reps_min times). pre(), when given,
+    runs before each timed region, outside it (the L2 flush). Returns the
+    list of elapsed milliseconds, each the max over ranks."""
     out = []
     t_end = time.perf_counter() + seconds
     while len(out) < reps_min or time.perf_counter() < t_end:
         if barrier:
             barrier()
+        if pre:
+            pre()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -316,8 +357,9 @@ def run_ours(args):
     n_launch = (K + BB - 1) // BB
 
     def batched(i):  # up to BB consecutive sets (one batch each) in one launch
-        nbat = min(BB, K - i * BB)
-        v = (i * BB) % sets.n
+        j, r = divmod(i, n_launch)   # graph j of the rotation, launch r in it
+        nbat = min(BB, K - r * BB)
+        v = (j * K + r * BB) % sets.n
         if v + nbat > sets.n:
             v = 0
         tbs.qsa_select_step_batched(sets.q32[v:v + nbat], sets.kb[v:v + nbat], w.n_kv, w.k,
@@ -340,18 +382,14 @@ def run_ours(args):
         for i in range(W):
             step(i)
     torch.cuda.synchronize()
+    plan = tbs.qsa_arm().split("last call on this thread: ", 1)[-1]
 
-    # CUDA graphs of exactly K calls each (captured once, replayed)
-    graphs = {name: graph_of(torch, stream, fn, cnt) for name, fn, cnt in
-              (("step", step, K), ("score", score_only, K), ("select", select_only, K),
-               ("convert", convert_only, K), ("batched", batched, n_launch))}
-    replays = {}
-    for name, g in graphs.items():  # upload + one untimed replay, on the timed stream
-        def rp(g=g):
-            with torch.cuda.stream(stream):
-                g.replay()
-        replays[name] = rp
-        rp()
+    # CUDA graphs of exactly K calls each (captured once, replayed in turn
+    # over all the rotating sets)
+    replays = {name: rotating_replay(torch, stream, fn, cnt, n_sets) for name, fn, cnt, n_sets in
+               (("step", step, K, sets.n), ("score", score_only, K, sets.n),
+                ("select", select_only, K, sets.n), ("convert", convert_only, K, sets.n),
+                ("batched", batched, n_launch, -(-sets.n // K) * n_launch))}
     torch.cuda.synchronize()
 
     uuid = None
@@ -392,12 +430,13 @@ def run_ours(args):
                 "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     if step_launches == 1:
-        roof["traffic"] = traffic_for("fused_step_kernel", w)
-        roof["kernel"] = "fused_step_kernel (qsa_select_step: one launch per step)"
+        kname = plan.split(": ", 1)[-1].split(" ")[0]
+        roof["traffic"] = traffic_for(kname, w)
+        roof["kernel"] = f"{kname} (qsa_select_step: one launch per step)"
     else:
         roof["traffic"] = None
-        roof["kernel"] = (f"qsa_select_step as {step_launches} chained launches (convert, "
-                          "score_tc, tail, select) taken as one step")
+        roof["kernel"] = f"qsa_select_step as {step_launches} chained launches taken as one step"
+    roof["plan"] = plan
     roof["peak_source"] = f"{peak_src} (fp16 dense taken equal to the measured bf16 burst)"
     roof["algorithmic"] = {"flops": step_flops, "bytes": step_bytes,
                            "t_roofline_us": max(t_flop, t_byte) * 1e6, "t_launch_us": t_step * 1e6}
@@ -446,6 +485,10 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
     }
+    if not args.no_per_config:
+        res["per_config"] = run_per_config(
+            torch, tbs, device, stream, peaks, peak_src, K, W,
+            0.0 if args.no_cpu_baseline else args.per_config_cpu_seconds, barrier if dist else None)
     if not args.no_split:
         res["split_reduce"] = run_split(torch, tbs, device, stream, peaks, peak_src, K,
                                         barrier if dist else None)
@@ -456,6 +499,129 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def step_plan(tbs, w):
+    """(with_q16, launches) of qsa_select_step on workload w: the fp16 query
+    buffer is passed only where it changes the library's plan (large problems
+    run the separate kernels, which need it)."""
+    n0 = tbs.qsa_select_step_launches(w.nq, w.H, w.D, w.n_kv, w.k, w.block, with_q16=False)
+    n1 = tbs.qsa_select_step_launches(w.nq, w.H, w.D, w.n_kv, w.k, w.block, with_q16=True)
+    return (True, n1) if n1 != n0 else (False, n0)
+
+
+def step_roofline(w, t_step, peaks, with_q16):
+    """Roofline of one step of workload w measured at t_step seconds: the
+    larger of its FLOP time at the fp16 tensor peak and its byte time at the
+    HBM peak (algorithmic work: every block's FLOPs, each input read and each
+    output written once, plus the fp16 query copy when the plan writes one)."""
+    flops = 2.0 * w.nq * w.H * w.D * w.nb
+    nbytes = 4.0 * w.nq * w.H * w.D + 2.0 * w.nb * w.D + 4.0 * w.nq * w.nb + 4.0 * w.nq * w.k
+    if with_q16:
+        nbytes += 2.0 * w.nq * w.H * w.D
+    t_flop = flops / (peaks["bf16_tflops"] * 1e12)
+    t_byte = nbytes / (peaks["hbm_gbs"] * 1e9)
+    if t_flop >= t_byte:
+        r = {"bound": "tensor", "achieved": flops / t_step / 1e12, "peak": peaks["bf16_tflops"],
+             "unit": "TFLOP/s"}
+    else:
+        r = {"bound": "hbm", "achieved": nbytes / t_step / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["t_roofline_us"] = max(t_flop, t_byte) * 1e6
+    r["flops"] = flops
+    r["bytes"] = nbytes
+    return r
+
+
+PER_CONFIG = [w.name for w in qi.WORKLOADS + qi.DECODE_WORKLOADS]
+
+
+def run_per_config(torch, tbs, device, stream, peaks, peak_src, K, W, cpu_budget, barrier):
+    """Every workload and the decode shapes through qsa_select_step, each
+    timed two ways: cold (a CUDA graph of K steps over rotating input/output
+    sets larger than twice L2, so every step reads from HBM) and warm (K
+    steps on one L2-resident set). Per entry: ms per step, query*blocks/s,
+    the roofline of the cold number (and the warm one's fraction), and a
+    bounded CPU-oracle sample (rank 0 of a one-rank job)."""
+    from oracle import qsa_oracle as orc
+    out = {}
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+
+    def flush():  # write a buffer larger than L2, outside the timed region
+        with torch.cuda.stream(stream):
+            flush_buf.fill_(1.0)
+    for name in PER_CONFIG:
+        w = qi.BY_NAME[name]
+        with_q16, launches = step_plan(tbs, w)
+        # K distinct sets at most (each touched once per replay, after an L2
+        # flush), or fewer large ones that add up to more than twice L2
+        per = Sets.bytes_per_set(w)
+        n_sets = min(K, max(3, math.ceil(2 * L2_BYTES / per)))
+        sets = Sets(torch, tbs, w, device, n_sets * per, rank, max_distinct=8, min_sets=3)
+
+        def step(i, sets=sets, w=w, with_q16=with_q16):
+            v = i % sets.n
+            tbs.qsa_select_step(sets.q32[v], sets.kb[v], w.n_kv, w.k, w.block,
+                                q16=sets.q16[v] if with_q16 else None,
+                                scores=sets.scores[v], ids=sets.ids[v])
+
+        def step_warm(i, sets=sets, w=w, with_q16=with_q16):
+            tbs.qsa_select_step(sets.q32[0], sets.kb[0], w.n_kv, w.k, w.block,
+                                q16=sets.q16[0] if with_q16 else None,
+                                scores=sets.scores[0], ids=sets.ids[0])
+
+        with torch.cuda.stream(stream):
+            for i in range(W):
+                step(i)
+        torch.cuda.synchronize()
+        res = {}
+        for label, fn in (("cold", step), ("warm", step_warm)):
+            g = graph_of(torch, stream, fn, K)
+
+            def rp(g=g):
+                with torch.cuda.stream(stream):
+                    g.replay()
+            rp()
+            torch.cuda.synchronize()
+            ms = statistics.median(time_region(torch, stream, rp, 5, 0.25, barrier,
+                                               pre=flush if label == "cold" else None))
+            res[label] = ms / K
+            del g
+        t_cold = res["cold"] / 1e3
+        t_warm = res["warm"] / 1e3
+        roof = step_roofline(w, t_cold, peaks, with_q16)
+        roof["peak_source"] = peak_src
+        entry = {"nq": w.nq, "H": w.H, "D": w.D, "n_kv": w.n_kv, "nb": w.nb, "k": w.k,
+                 "launches_per_step": launches,
+                 "ms_per_step": res["cold"], "value": world * w.nq * w.nb / t_cold,
+                 "unit": UNIT, "roofline": roof,
+                 "warm": {"ms_per_step": res["warm"], "value": world * w.nq * w.nb / t_warm,
+                          "roofline_frac": roof["t_roofline_us"] / 1e6 / t_warm},
+                 "l2": f"cold: {sets.n} rotating sets ({sets.n * sets.per_set_bytes / 2**20:.0f} MiB); "
+                       f"warm: one set"}
+        if rank == 0 and world == 1 and cpu_budget > 0:
+            entry["cpu_baseline"] = cpu_sample(orc, w, cpu_budget)
+        out[name] = entry
+        del sets
+        torch.cuda.empty_cache()
+    return out
+
+
+def cpu_sample(orc, w, seconds):
+    """The oracle on a bounded sample of workload w (whole batches when
+    nq <= 256, else the first 256 queries), repeated for about `seconds`."""
+    nq_s = min(w.nq, 256)
+    q32, _ = qi.make_f32_inputs(w)
+    _, kb = qi.make_inputs(w)
+    n, t0 = 0, time.perf_counter()
+    while n < 1 or time.perf_counter() - t0 < seconds:
+        oracle_step(orc, w, q32, kb, nq_s)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": n * nq_s * w.nb / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} runs of {nq_s} of the {w.nq} queries in {dt:.1f} s"}
 
 
 SPLIT_WORKLOAD = "split_g4_r8_c128_b2048"

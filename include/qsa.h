@@ -63,9 +63,14 @@ int qsa_abi_version(void);
 /* Static, NUL-terminated name of a status code. */
 const char* qsa_status_str(qsa_status status);
 
-/* Static, NUL-terminated description of the kernels that run (the "arm"),
- * so that no other path can pass for this one (after Strata pull request 228,
- * part 1, which prints the arm that ran). */
+/* NUL-terminated description of the arm (the kernels this library runs),
+ * followed by the plan the last launching call on this thread ran: the
+ * number of launches and each kernel by name, in order (for example one
+ * select_step_kernel launch, or a chain of convert, score, tail and select
+ * kernels), or "none" before any such call. So a fallback cannot pass for
+ * the fast path (after Strata pull request 228, part 1, which prints the arm
+ * that ran). The text lives in thread-local storage: valid until the next
+ * qsa_arm() call on the same thread. */
 const char* qsa_arm(void);
 
 /* Static text of the last CUDA error that made a call of this thread return
@@ -263,8 +268,13 @@ qsa_status qsa_select_step_host_packed(const void* in_host, int32_t nq, int32_t 
  *                             bytes (0 when B <= 128: NULL allowed). Its first
  *                             bytes hold arrival counters that must be zero
  *                             before the first call (zero-fill it once); every
- *                             call leaves them zero again. Calls that may run
- *                             at the same time need separate workspaces.
+ *                             call that completes leaves them zero again. A
+ *                             call whose staging wait ran out (bit 3 of the
+ *                             status word, QSA_ERR_TIMEOUT from
+ *                             qsa_device_status) returns early and may leave
+ *                             them nonzero: zero-fill the workspace again
+ *                             before its next use. Calls that may run at the
+ *                             same time need separate workspaces.
  * Arithmetic (fixed, so results are reproducible bit for bit on any GB300):
  * the blocks are reduced in chunks of 128 (the scales of a chunk staged on
  * chip), each chunk in runs of 32 blocks; in a run, sum and out accumulate
@@ -277,6 +287,10 @@ qsa_status qsa_select_step_host_packed(const void* in_host, int32_t nq, int32_t 
  * C % 4 == 0, R * C <= 4096, G <= 65535.
  * Errors: QSA_ERR_INVALID_ARG (a NULL buffer, B < 1, R < 1, G < 0, a
  * workspace smaller than required), QSA_ERR_UNSUPPORTED_GEOMETRY, QSA_ERR_MISALIGNED.
+ * Order of the checks: the sizes first (INVALID_ARG for negative or zero
+ * sizes, then UNSUPPORTED_GEOMETRY), then G == 0 returns QSA_OK without
+ * looking at any pointer, then the pointers (INVALID_ARG for a NULL buffer
+ * or a short workspace), then their alignment (MISALIGNED).
  */
 size_t qsa_split_reduce_workspace_bytes(int32_t G, int32_t R, int32_t B, int32_t C);
 qsa_status qsa_split_reduce(const float* partial_max, const float* partial_sum,
@@ -302,8 +316,16 @@ qsa_status qsa_split_reduce(const float* partial_max, const float* partial_sum,
  * Calls that may run at the same time on one device (other streams or other
  * host threads) share the array and race: serialise them.
  * The first call on each device looks up the array's address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture on the device.
+ * (cudaGetSymbolAddress, with that device current) and keeps it for the
+ * life of the process; make that first call before any stream capture on
+ * the device. The kept address assumes that the device's primary context
+ * lives as long as the process: after cudaDeviceReset (or a release and
+ * re-creation of the primary context) the array may move, so do not call
+ * this entry point on that device again in the same process.
+ * Order of the checks: the sizes as for qsa_split_reduce, then a workspace
+ * need above QSA_SPLIT_STATIC_SCRATCH_BYTES (UNSUPPORTED_GEOMETRY), then
+ * G == 0 returns QSA_OK without looking at any pointer, then the pointers
+ * (INVALID_ARG) and their alignment (MISALIGNED).
  */
 #define QSA_SPLIT_STATIC_SCRATCH_BYTES (4u << 20)
 qsa_status qsa_split_reduce_static(const float* partial_max, const float* partial_sum,

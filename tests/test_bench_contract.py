@@ -50,12 +50,16 @@ def test_traffic_reported_only_for_measured_sources(monkeypatch):
     import bench
     import qsa_inputs as qi
     w = qi.BY_NAME["long128k_nq256_h8_d128_kv131072"]
-    rec = bench.NCU_TRAFFIC["fused_step_kernel"]
-    assert bench.traffic_for("fused_step_kernel", w) == rec["bytes_per_launch"]
-    assert bench.traffic_for("fused_step_kernel", qi.BY_NAME["mid_nq256_h8_d128_kv32805"]) is None
+    name = next(n for n, r in bench.NCU_TRAFFIC.items() if r["workload"] == w.name)
+    rec = bench.NCU_TRAFFIC[name]
+    # the record is reported while the kernel's sources are the captured ones
+    monkeypatch.setattr(bench, "kernel_source_sha", lambda names: rec["source_sha"])
+    assert bench.traffic_for(name, w) == rec["bytes_per_launch"]
+    assert bench.traffic_for(name, qi.BY_NAME["mid_nq256_h8_d128_kv32805"]) is None
     assert bench.traffic_for("no_such_kernel", w) is None
+    # and not once they have changed
     monkeypatch.setattr(bench, "kernel_source_sha", lambda names: "0" * 16)
-    assert bench.traffic_for("fused_step_kernel", w) is None
+    assert bench.traffic_for(name, w) is None
 
 
 def test_units_and_rates():

@@ -179,12 +179,18 @@ def pin_partition(part_fn):
                 assert n_full * block <= n_kv < (n_full + 1) * block
 
 
-def pin_hand_example(scores_fn, tail_fn, select_fn):
+def pin_hand_example(scores_fn, tail_fn, select_fn, S_fn=orc.abs_product_sum_f64,
+                     bound_fn=orc.error_bound):
     g = _load_golden("hand_example.txt")
     q = np.array(g["q"], dtype=np.float16)
     kb = np.array(g["kb"], dtype=np.float16)
     s = scores_fn(q, kb, g["n_kv"], g["block"])
     assert np.array_equal(s[:, :2], np.array(g["full_scores"]))
+    # S and the bound B, worked by hand in the fixture from the printed formula
+    S = S_fn(q, kb, g["n_kv"], g["block"])
+    assert np.array_equal(S[:, :2], np.array(g["S_full"]))
+    B = bound_fn(S[:, :2], s[:, :2])
+    assert np.allclose(B, np.array(g["B_full"]), rtol=1e-13, atol=0.0)
     tail = tail_fn(q, kb, g["n_kv"], g["block"])
     assert tail.dtype == np.float32
     assert np.array_equal(tail, np.array(g["tail"], dtype=np.float32))
@@ -319,6 +325,30 @@ def test_bound_checker_negative_control():
         s = s_ref.copy()
         s[0, -1] = float(np.nextafter(np.float32(s[0, -1]), np.float32(np.inf)))
         assert not orc.bound_report(s, s_ref, B)["ok"]
+
+
+def test_bound_checker_at_the_hand_worked_bound():
+    """The checker passes an error just below the hand-worked B and fails one
+    just above it (golden hand example, full entries)."""
+    g = _load_golden("hand_example.txt")
+    s_ref = np.array(g["full_scores"], dtype=np.float64)
+    B_hand = np.array(g["B_full"], dtype=np.float64)
+    S = np.array(g["S_full"], dtype=np.float64)
+    B = orc.error_bound(S, s_ref)
+    for sign in (1.0, -1.0):
+        assert orc.bound_report(s_ref + sign * B_hand * (1 - 1e-9), s_ref, B)["ok"]
+        bad = orc.bound_report(s_ref + sign * B_hand * (1 + 1e-9), s_ref, B)
+        assert not bad["ok"] and bad["n_bad"] == B.size
+
+
+@pytest.mark.parametrize("name,value", [("BOUND_REL_S", 2.0 ** -9), ("BOUND_REL_S", 2.0 ** -7),
+                                        ("BOUND_REL_SCORE", 0.0), ("BOUND_REL_SCORE", 2.0 ** -24)])
+def test_planted_bound_mistakes_are_caught(monkeypatch, name, value):
+    """A wrong exponent on the S term or a dropped / shrunk |score| term in B
+    fails the hand-worked bound pin."""
+    monkeypatch.setattr(orc, name, value)
+    with pytest.raises(AssertionError):
+        pin_hand_example(orc.scores_f64, orc.tail_scores_f32, orc.select_topk)
 
 
 def test_selection_checker_controls():

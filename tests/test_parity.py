@@ -166,9 +166,10 @@ def test_fused_matches_separate_kernels(tbs):
 
 
 def test_large_step_paths_agree(tbs):
-    """On the 4096-query prefill shape the single-batch entry points run the
-    separate stages (convert, score + tail, select) and the batched entry
-    points the one fused kernel; both give the same bits."""
+    """On the 4096-query prefill shape every path gives the same bits: the
+    single-batch step (whatever plan it takes), the batched entry point (the
+    8-CTA fused kernel), and the separate stages called one by one
+    (conversion, score + tail, select)."""
     w = qi.BY_NAME["prefill_nq4096_h16_d128_kv131073"]
     q32, _ = qi.make_f32_inputs(w)
     _, kb = qi.make_inputs(w)
@@ -178,16 +179,41 @@ def test_large_step_paths_agree(tbs):
     _, s_f, i_f = tbs.qsa_select_step(dev(q32), kd, w.n_kv, w.k, w.block)
     s_b, i_b = tbs.qsa_score_select_batched(q16_s[None], kd, w.n_kv, w.k, w.block)
     s_1, i_1 = tbs.qsa_score_select(q16_s, kd, w.n_kv, w.k, w.block)
+    q16_c = tbs.qsa_f32_to_f16(dev(q32))
+    s_c = tbs.qsa_block_scores(q16_c, kd, w.n_kv, w.block)
+    i_c = tbs.qsa_select(s_c, w.k)
     torch.cuda.synchronize()
-    for s, i in ((s_f, i_f), (s_b[0], i_b[0]), (s_1, i_1)):
+    for s, i in ((s_f, i_f), (s_b[0], i_b[0]), (s_1, i_1), (s_c, i_c)):
         assert torch.equal(s.view(torch.int32), s_s.view(torch.int32))
         assert torch.equal(i, i_s)
     assert np.array_equal(q16_s.cpu().numpy().view(np.uint16), orc.f32_to_f16(q32).view(np.uint16))
-    # the launch plan the library reports for the two calls
-    assert tbs.qsa_select_step_launches(w.nq, w.H, w.D, w.n_kv, w.k, w.block, with_q16=True) == 4
-    assert tbs.qsa_select_step_launches(w.nq, w.H, w.D, w.n_kv, w.k, w.block, with_q16=False) == 1
+
+
+def test_arm_reports_the_plan_that_ran(tbs):
+    """qsa_arm() names the kernels the last call on this thread launched: the
+    one-tile-per-CTA step kernel for the 128K step, the 8-CTA fused kernel
+    for a batched launch, and the chain of separate kernels for a step too
+    large for either fused form; qsa_select_step_launches agrees."""
     h = qi.BY_NAME["long128k_nq256_h8_d128_kv131072"]
-    assert tbs.qsa_select_step_launches(h.nq, h.H, h.D, h.n_kv, h.k, h.block, with_q16=True) == 1
+    q32, _ = qi.make_f32_inputs(h)
+    _, kb = qi.make_inputs(h)
+    tbs.qsa_select_step(dev(q32), dev(kb), h.n_kv, h.k, h.block)
+    arm = tbs.qsa_arm()
+    assert "last call on this thread: 1 launch: select_step_kernel" in arm, arm
+    assert tbs.qsa_select_step_launches(h.nq, h.H, h.D, h.n_kv, h.k, h.block, with_q16=False) == 1
+    tbs.qsa_select_step_batched(dev(q32[None]), dev(kb), h.n_kv, h.k, h.block)
+    assert "1 launch: fused_step_kernel" in tbs.qsa_arm()
+    # 4096 queries of 16 heads over 3000 blocks: more than 16 tiles of 128
+    # blocks per query group and too many 8-CTA clusters -> the chain
+    nq, H, nb = 4096, 16, 3000
+    q, kb2 = qi.random_case_f32(nq, H, 128, nb, seed=77, scale=0.25)
+    q16 = torch.empty(q.shape, dtype=torch.float16, device="cuda")
+    tbs.qsa_select_step(dev(q), dev(kb2), nb * 64, 64, 64, q16=q16)
+    torch.cuda.synchronize()
+    arm = tbs.qsa_arm()
+    assert ("3 launches: convert_vec8_kernel -> score_tc_persistent_kernel -> "
+            "select_window_kernel") in arm, arm
+    assert tbs.qsa_select_step_launches(nq, H, 128, nb * 64, 64, 64, with_q16=True) == 3
 
 
 @pytest.mark.parametrize("nq,H,n_kv", [(1000, 8, 2500 * 64 + 5), (600, 16, 1900 * 64)])

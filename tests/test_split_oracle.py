@@ -5,6 +5,7 @@ direct softmax over the tokens, closed forms, a hand-worked example, and
 planted mistakes that the checks must catch.
 """
 import math
+import struct
 import os
 
 import numpy as np
@@ -182,3 +183,89 @@ def test_run_order_is_what_changes_the_bits():
         sro.RUN = old
     assert not np.array_equal(a, b)
     assert sro.bound_report(a, ref, bound)["ok"] and sro.bound_report(b, ref, bound)["ok"]
+
+
+# ------------------------------------ a second, scalar model of the procedure
+# Written from the statement of the fixed order (chunks of 128 blocks, each
+# in runs of 32; inside a run one rounded product then one rounded add per
+# block, from 0; runs added in order into the chunk partial, chunk partials
+# added in chunk order; one rounded division) and of the exponential (Cody
+# and Waite's reduction with ln 2 split, the degree-7 Taylor polynomial in
+# Horner form, exact scaling by 2^n, flush below -86), in plain Python
+# floats, each operation's binary64 result rounded to binary32 with struct.
+# For +, -, * and / on binary32 operands the binary64 result rounded once
+# more to binary32 equals the correctly rounded binary32 result (53 >= 2*24
+# + 2), so this is IEEE binary32 arithmetic, computed another way.
+def _f32(x):
+    return struct.unpack("<f", struct.pack("<f", x))[0]
+
+
+_LN2_HI = 0.693145751953125                     # 16 significant bits: n * LN2_HI is exact
+_LN2_LO = _f32(math.log(2.0) - _LN2_HI)
+_LOG2E = _f32(1.0 / math.log(2.0))
+
+
+def _exp_scalar(x):
+    if x < -86.0:
+        return 0.0
+    n = float(round(_f32(x * _LOG2E)))           # Python's round() is half-to-even
+    t = _f32(_f32(x - _f32(n * _LN2_HI)) - _f32(n * _LN2_LO))
+    p = _f32(1.0 / math.factorial(7))
+    for k in range(6, -1, -1):
+        p = _f32(_f32(p * t) + _f32(1.0 / math.factorial(k)))
+    return _f32(p * math.ldexp(1.0, int(n)))
+
+
+def split_reduce_scalar(pm, ps, po, chunk=128, run=32):
+    G, R, B = pm.shape
+    C = po.shape[3]
+    out = np.zeros((G, R, C), np.float32)
+    for g in range(G):
+        for r in range(R):
+            m = max(float(v) for v in pm[g, r])
+            scale = [_exp_scalar(_f32(float(pm[g, r, b]) - m)) for b in range(B)]
+            tot_s, tot_o = 0.0, [0.0] * C
+            for c0 in range(0, B, chunk):
+                part_s, part_o = 0.0, [0.0] * C
+                for r0 in range(c0, min(B, c0 + chunk), run):
+                    run_s, run_o = 0.0, [0.0] * C
+                    for b in range(r0, min(B, r0 + run)):
+                        run_s = _f32(run_s + _f32(scale[b] * float(ps[g, r, b])))
+                        for c in range(C):
+                            run_o[c] = _f32(run_o[c] + _f32(scale[b] * float(po[g, r, b, c])))
+                    part_s = _f32(part_s + run_s)
+                    part_o = [_f32(a + v) for a, v in zip(part_o, run_o)]
+                tot_s = _f32(tot_s + part_s)
+                tot_o = [_f32(a + v) for a, v in zip(tot_o, part_o)]
+            out[g, r] = [_f32(v / tot_s) for v in tot_o]
+    return out
+
+
+def test_exp_scalar_model_equals_exp_f32():
+    """The two exponentials agree bit for bit (reduction boundaries, the flush
+    threshold and random arguments included)."""
+    rng = np.random.default_rng(8)
+    x = np.concatenate([-rng.exponential(4.0, size=3000), np.linspace(-86.0, 0.0, 2001),
+                        -np.arange(0, 125) * math.log(2.0), [-85.999, -86.0, -86.001, -0.0]])
+    x = x.astype(np.float32)
+    got = np.array([_exp_scalar(float(v)) for v in x], np.float32)
+    assert np.array_equal(got.view(np.uint32), sro.exp_f32(x).view(np.uint32))
+
+
+@pytest.mark.parametrize("G,R,B,C", [(1, 1, 1, 4), (1, 2, 31, 4), (1, 3, 33, 8), (2, 2, 100, 4),
+                                     (1, 2, 129, 8), (1, 1, 257, 4), (1, 2, 300, 12)])
+def test_f32_procedure_equals_scalar_model(G, R, B, C):
+    """split_reduce_f32 equals the scalar model bit for bit, on block counts
+    that are and are not multiples of the run (32) and chunk (128) sizes."""
+    pm, ps, po = qi.split_random_case(G, R, B, C, seed=1000 + B)
+    got = sro.split_reduce_f32(pm, ps, po)
+    want = split_reduce_scalar(pm, ps, po)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_scalar_model_catches_a_changed_order():
+    """The scalar model sees a different run length (its bits differ), so the
+    equality above pins the order, not just the value."""
+    pm, ps, po = qi.split_random_case(1, 2, 300, 12, seed=1300)
+    assert not np.array_equal(split_reduce_scalar(pm, ps, po, run=32),
+                              split_reduce_scalar(pm, ps, po, run=128))

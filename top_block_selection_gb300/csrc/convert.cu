@@ -57,6 +57,7 @@ cudaError_t launch_convert(const float* src, uint16_t* dst, int64_t n, const Dev
     if (n8 > 0) {
       int64_t blocks = (n8 + kConvThreads - 1) / kConvThreads;
       if (blocks > wave * 4) blocks = wave * 4;
+      plan_add("convert_vec8_kernel");
       cudaError_t e = launch_pdl(convert_vec8_kernel, dim3(static_cast<unsigned>(blocks)),
                                  dim3(kConvThreads), 0, stream,
                                  reinterpret_cast<const float4*>(src), reinterpret_cast<uint4*>(dst),
@@ -69,6 +70,7 @@ cudaError_t launch_convert(const float* src, uint16_t* dst, int64_t n, const Dev
   if (rest > 0) {
     int64_t blocks = (rest + kConvThreads - 1) / kConvThreads;
     if (blocks > wave * 4) blocks = wave * 4;
+    plan_add("convert_scalar_kernel");
     return launch_pdl(convert_scalar_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kConvThreads),
                       0, stream, src + done, reinterpret_cast<__half*>(dst) + done, rest);
   }

@@ -794,6 +794,7 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
   const bool f32q = p.q32 != nullptr;
   const void* fn = fused_kernel_for(p.H, f32q, lean);
   if (fn == nullptr) return cudaErrorInvalidValue;
+  plan_add(lean ? "fused_step_kernel (8-CTA clusters, lean form)" : "fused_step_kernel (8-CTA clusters)");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kFThreads);

@@ -4,9 +4,15 @@
 #include "qsa.h"
 
 #include <cstdint>
+#include <cstdio>
 #include <cuda_runtime.h>
 
 #include "qsa_internal.h"
+
+namespace qsa {
+void plan_begin();
+void plan_add(const char* kernel);
+}  // namespace qsa
 
 namespace {
 
@@ -22,6 +28,12 @@ cudaStream_t as_cuda(qsa_stream_t s) { return reinterpret_cast<cudaStream_t>(s);
 
 thread_local const char* t_last_cuda_error = "no error";
 
+// The kernels the last call on this thread launched, in order (static names).
+constexpr int kPlanMax = 8;
+thread_local const char* t_plan[kPlanMax];
+thread_local int t_plan_n = 0;
+thread_local bool t_plan_any = false;
+
 qsa_status cuda_fail(cudaError_t e) {
   t_last_cuda_error = cudaGetErrorString(e);
   return QSA_ERR_CUDA;
@@ -29,13 +41,15 @@ qsa_status cuda_fail(cudaError_t e) {
 
 qsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QSA_OK : cuda_fail(e); }
 
-// Returns the current device's info, or an error status.
-qsa_status device_or_error(const DeviceInfo** out) {
+// Returns the current device's info, or an error status. Entry points that
+// launch pass launching = true, which starts this thread's plan record.
+qsa_status device_or_error(const DeviceInfo** out, bool launching = true) {
   cudaError_t e = cudaSuccess;
   const DeviceInfo* d = qsa::current_device(&e);
   if (!d) return cuda_fail(e);
   if (!d->supported) return QSA_ERR_UNSUPPORTED_ARCH;
   *out = d;
+  if (launching) qsa::plan_begin();
   return QSA_OK;
 }
 
@@ -98,6 +112,16 @@ qsa_status run_separate(const uint16_t* q, const uint16_t* kb, int32_t nq, int32
 
 }  // namespace
 
+namespace qsa {
+void plan_begin() {
+  t_plan_n = 0;
+  t_plan_any = true;
+}
+void plan_add(const char* kernel) {
+  if (t_plan_n < kPlanMax) t_plan[t_plan_n++] = kernel;
+}
+}  // namespace qsa
+
 extern "C" {
 
 int qsa_abi_version(void) { return QSA_ABI_VERSION; }
@@ -118,9 +142,21 @@ const char* qsa_status_str(qsa_status s) {
 }
 
 const char* qsa_arm(void) {
-  return "sm_103a: TMA + tcgen05.mma kind::f16 (M128, fp32 in TMEM) scorer with fused "
-         "ReLU/head-sum epilogue; fp32 pinned-order tail kernel (+1e9); radix top-k select "
-         "(block-index tie-break); cvt.rn fp32->fp16 stage";
+  thread_local char buf[1024];
+  int n = snprintf(buf, sizeof buf,
+                   "sm_103a: TMA + tcgen05.mma kind::f16 (M128, fp32 in TMEM) scorer with fused "
+                   "ReLU/head-sum epilogue; fp32 pinned-order tail (+1e9); radix top-k select "
+                   "(block-index tie-break); cvt.rn fp32->fp16 stage | last call on this thread: ");
+  if (!t_plan_any) {
+    snprintf(buf + n, sizeof buf - n, "none");
+  } else if (t_plan_n == 0) {
+    snprintf(buf + n, sizeof buf - n, "no launch");
+  } else {
+    n += snprintf(buf + n, sizeof buf - n, "%d launch%s: ", t_plan_n, t_plan_n == 1 ? "" : "es");
+    for (int i = 0; i < t_plan_n && n < static_cast<int>(sizeof buf); ++i)
+      n += snprintf(buf + n, sizeof buf - n, "%s%s", i ? " -> " : "", t_plan[i]);
+  }
+  return buf;
 }
 
 int64_t qsa_num_blocks(int64_t n_kv, int32_t block) {
@@ -170,10 +206,12 @@ qsa_status qsa_score_select(const uint16_t* q, const uint16_t* kb, int32_t nq, i
   if (g.nb > 0 && (!q || !kb)) return QSA_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
-  if (g.nb > 0 && use_separate(nq, H, *dev))
-    return run_separate(q, kb, nq, H, D, g, k, scores, ids, *dev, as_cuda(stream));
   qsa::FusedProblem p{nullptr, q,       nullptr,  kb, scores, ids, nq, H, D, g.nb, g.n_full,
                       g.has_tail, k, 1, 0};
+  if (g.nb > 0 && qsa::step_supported(nq, H, D, g.nb, g.n_full, k, *dev))
+    return from_cuda(qsa::launch_step(p, *dev, as_cuda(stream)));
+  if (g.nb > 0 && use_separate(nq, H, *dev))
+    return run_separate(q, kb, nq, H, D, g, k, scores, ids, *dev, as_cuda(stream));
   return from_cuda(qsa::launch_fused(p, *dev, as_cuda(stream)));
 }
 
@@ -191,6 +229,11 @@ qsa_status qsa_select_step(const float* q32, uint16_t* q16, const uint16_t* kb, 
   if (!aligned(q32, 16) || !aligned(q16, 16)) return QSA_ERR_MISALIGNED;
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  if (g.nb > 0 && qsa::step_supported(nq, H, D, g.nb, g.n_full, k, *dev)) {
+    qsa::FusedProblem p{q32, nullptr, q16, kb, scores, ids, nq, H, D, g.nb, g.n_full,
+                        g.has_tail, k, 1, 0};
+    return from_cuda(qsa::launch_step(p, *dev, as_cuda(stream)));
+  }
   if (q16 && g.nb > 0 && use_separate(nq, H, *dev)) {
     cudaStream_t s = as_cuda(stream);
     const int64_t n = static_cast<int64_t>(nq) * H * D;
@@ -210,7 +253,8 @@ int32_t qsa_select_step_launches(int32_t nq, int32_t H, int32_t D, int64_t n_kv,
   if (nb > qsa::kMaxSelectNb || static_cast<int64_t>(nq) * H > 0x7FFFFFFFLL) return -1;
   if (nq == 0 || nb == 0) return 0;
   const DeviceInfo* dev = nullptr;
-  if (device_or_error(&dev) != QSA_OK) return -1;
+  if (device_or_error(&dev, false) != QSA_OK) return -1;
+  if (qsa::step_supported(nq, H, D, nb, n_kv / block, k, *dev)) return 1;
   if (!with_q16 || !use_separate(nq, H, *dev)) return 1;
   // convert (nq * H * D is a multiple of 8: one vector launch), the score
   // kernel when there are full blocks, the tail kernel when there is a tail,
@@ -414,7 +458,7 @@ qsa_status qsa_selftest_bounded_wait(uint64_t timeout_ns, qsa_stream_t stream) {
 
 qsa_status qsa_device_status(int clear, uint32_t* bits, qsa_stream_t stream) {
   const DeviceInfo* dev = nullptr;
-  qsa_status st = device_or_error(&dev);
+  qsa_status st = device_or_error(&dev, false);
   if (st != QSA_OK) return st;
   cudaError_t e = cudaStreamSynchronize(as_cuda(stream));
   if (e != cudaSuccess) return cuda_fail(e);

@@ -49,6 +49,13 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
 
+// The launch plan of the last library call on this thread, which qsa_arm()
+// reports: each entry point clears it (plan_begin) and every launcher
+// appends the kernel it launched (plan_add, a static string), so a chain of
+// separate kernels or a different form of a kernel cannot pass for another.
+void plan_begin();
+void plan_add(const char* kernel);
+
 // Per-TU one-time kernel attribute setup, called from current_device().
 cudaError_t init_score_kernels(const DeviceInfo& dev);
 cudaError_t init_select_kernels(const DeviceInfo& dev);
@@ -90,6 +97,14 @@ cudaError_t init_fused_kernels(const DeviceInfo& dev);
 // CTAs the fused kernel would launch for one batch of nq queries of H heads.
 int64_t fused_blocks(int32_t nq, int32_t H, const DeviceInfo& dev);
 cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStream_t stream);
+
+// The one-tile-per-CTA step kernel (step.cu): single-batch steps whose
+// blocks fit one 16-CTA cluster per query group and whose rows' keys fit the
+// dead query tile. step_supported says whether it takes a problem.
+cudaError_t init_step_kernels(const DeviceInfo& dev);
+bool step_supported(int32_t nq, int32_t H, int32_t D, int64_t nb, int64_t n_full, int32_t k,
+                    const DeviceInfo& dev);
+cudaError_t launch_step(const FusedProblem& p, const DeviceInfo& dev, cudaStream_t stream);
 
 cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k, int32_t* ids,
                           const DeviceInfo& dev, cudaStream_t stream);

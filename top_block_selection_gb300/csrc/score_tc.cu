@@ -522,6 +522,7 @@ cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStre
       PersistArgs pa{m_tiles, m_tiles * n_tiles};
       const dim3 pgrid(static_cast<unsigned>(std::min<int64_t>(dev.sm_count, pa.tiles)));
       const dim3 pblock(kPThreads);
+      plan_add("score_tc_persistent_kernel");
       cudaError_t e = cudaErrorInvalidValue;
       switch (p.H) {
         case 1: e = launch_pdl(score_tc_persistent_kernel<1>, pgrid, pblock, psmem, stream, tm_kb, tm_q, a, pa); break;
@@ -536,6 +537,7 @@ cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStre
       if (p.nq > 0 && p.has_tail) {
         const int q_per_block = kTailThreads / p.H;
         const int64_t grid = (p.nq + q_per_block - 1) / q_per_block;
+        plan_add("tail_kernel");
         return launch_pdl(tail_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTailThreads), 0,
                           stream, reinterpret_cast<const __half*>(p.q),
                           reinterpret_cast<const __half*>(p.kb) + (p.nb - 1) * p.D, p.scores,
@@ -547,6 +549,7 @@ cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStre
     if (smem > static_cast<size_t>(dev.max_smem_optin)) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(m_tiles), static_cast<unsigned>(n_tiles));
     const dim3 block(kScoreThreads);
+    plan_add("score_tc_kernel");
     cudaError_t e;
     switch (p.H) {
       case 1: e = launch_pdl(score_tc_kernel<1>, grid, block, smem, stream, tm_kb, tm_q, a); break;
@@ -562,6 +565,7 @@ cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStre
   if (p.nq > 0 && p.has_tail) {
     const int q_per_block = kTailThreads / p.H;
     const int64_t grid = (p.nq + q_per_block - 1) / q_per_block;
+    plan_add("tail_kernel");
     return launch_pdl(tail_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTailThreads), 0, stream,
                       reinterpret_cast<const __half*>(p.q),
                       reinterpret_cast<const __half*>(p.kb) + (p.nb - 1) * p.D, p.scores, p.nq,

@@ -116,6 +116,7 @@ cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k
   if (nb >= 1 && nb <= 16 * kWinThreads && k <= 1024) {
     const size_t smem = select_window_bytes(k);
     const dim3 grid(static_cast<unsigned>(nq)), block(kWinThreads);
+    plan_add("select_window_kernel");
     if (nb <= 8 * kWinThreads)
       return launch_pdl(select_window_kernel<8>, grid, block, smem, stream, scores, nb, k, ids);
     if (nb <= 12 * kWinThreads)
@@ -128,6 +129,7 @@ cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k
   while (groups > 1 && static_cast<size_t>(groups) * per > room) groups >>= 1;
   if (per > room) return cudaErrorInvalidValue;
   const int64_t grid = (static_cast<int64_t>(nq) + groups - 1) / groups;
+  plan_add("select_kernel");
   return launch_pdl(select_kernel, dim3(static_cast<unsigned>(grid)), dim3(groups * 32 * kSelG),
                     groups * per, stream, scores, nq, nb, k, ids);
 }

@@ -806,4 +806,148 @@ __device__ void select_row_g(const uint32_t* keys, int nb, int k, int32_t* __res
   for (int j = kk + gtid; j < k; j += T) out[j] = -1;
 }
 
+
+// ------------------------------------- narrow window select, keys in smem
+// The top-k of one row whose keys[0..nb) are in shared memory, by a group of
+// T threads (whole warps), with a first digit of kSelNwBins bins of 1/64
+// octave measured down from an anchor A: the largest key other than
+// keys[skip] (skip < 0: the largest key). bin(key) = 0 for key >= A,
+// otherwise (A - key) >> kSelWinShift; bins from kSelNwBins down are below
+// the window and not counted. Keys above A (at most keys[skip]) share bin 0
+// with the keys just below A; every bin is ordered by the full key, so the
+// result does not depend on the anchor: only whether the window holds the
+// k-th largest key does. One warp scans the bins. Dense score rows put the
+// k-th key within a few octaves of the top, in a bin of a few keys: the
+// search ends after one histogram. Otherwise (the k-th key below the window,
+// more than kSelBinMax keys in its bin, or k >= nb) the function returns
+// false having written only scratch, and the caller runs select_row_g.
+// Scratch: hist >= 2 * kSelNwBins words (16-byte aligned), cand kSelBinMax,
+// sel and sel_bin k each. Ends without a barrier after the last read of
+// scratch; the caller synchronises before reusing it.
+constexpr int kSelNwBins = 256;
+
+struct NwShared {
+  uint32_t wmax[8];
+  uint32_t bdig, above, cnt, n_cand, ok;
+};
+
+__device__ __forceinline__ uint32_t nw_bin(uint32_t key, uint32_t anchor) {
+  return key >= anchor ? 0u : (anchor - key) >> kSelWinShift;
+}
+
+template <int T>
+__device__ bool select_row_narrow(const uint32_t* keys, int nb, int k, int skip,
+                                  int32_t* __restrict__ out, uint32_t* hist, uint64_t* cand,
+                                  uint64_t* sel, uint32_t* sel_bin, NwShared& sh, int gtid,
+                                  int bar_id) {
+  constexpr int kW = T / 32;
+  static_assert(kW >= 1 && kW <= 8, "1 to 8 warps per row");
+  const int lane = gtid & 31;
+  if (k >= nb) return false;
+  uint32_t* excl = hist + kSelNwBins;
+  // the anchor: the row's largest key other than keys[skip]
+  uint32_t m = 0;
+  for (int i = gtid; i < nb; i += T) {
+    const uint32_t kv = keys[i];
+    if (i != skip) m = max(m, kv);
+  }
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  if (lane == 0) sh.wmax[gtid >> 5] = m;
+  for (int i = gtid; i < kSelNwBins; i += T) hist[i] = 0u;
+  if (gtid == 0) sh.n_cand = 0;
+  group_sync<T>(bar_id);
+  uint32_t A = 0;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) A = max(A, sh.wmax[w]);
+  for (int i = gtid; i < nb; i += T) {
+    const uint32_t d = nw_bin(keys[i], A);
+    if (d < kSelNwBins) atomicAdd(&hist[d], 1u);
+  }
+  group_sync<T>(bar_id);
+  if (gtid < 32) {
+    // lane l: bins [8l, 8l + 8), top (bin 0) first
+    uint32_t c[8];
+    const uint4 v0 = *reinterpret_cast<const uint4*>(hist + 8 * lane);
+    const uint4 v1 = *reinterpret_cast<const uint4*>(hist + 8 * lane + 4);
+    c[0] = v0.x; c[1] = v0.y; c[2] = v0.z; c[3] = v0.w;
+    c[4] = v1.x; c[5] = v1.y; c[6] = v1.z; c[7] = v1.w;
+    uint32_t local = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) local += c[j];
+    uint32_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    const uint32_t kk = static_cast<uint32_t>(k);
+    uint32_t run = incl - local;
+    uint32_t e[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      e[j] = run;
+      if (run < kk && kk <= run + c[j]) {
+        sh.bdig = static_cast<uint32_t>(8 * lane + j);
+        sh.above = run;
+        sh.cnt = c[j];
+      }
+      run += c[j];
+    }
+    *reinterpret_cast<uint4*>(excl + 8 * lane) = make_uint4(e[0], e[1], e[2], e[3]);
+    *reinterpret_cast<uint4*>(excl + 8 * lane + 4) = make_uint4(e[4], e[5], e[6], e[7]);
+    if (lane == 31) sh.ok = incl >= kk ? 1u : 0u;
+  }
+  group_sync<T>(bar_id);
+  if (!sh.ok) return false;  // the k-th key lies below the window
+  const uint32_t bdig = sh.bdig, above = sh.above, cnt = sh.cnt;
+  const uint32_t need = static_cast<uint32_t>(k) - above;
+  const bool take_bin = cnt == need;
+  if (!take_bin && cnt > static_cast<uint32_t>(kSelBinMax)) return false;
+  // Winners (bins above the boundary, and the boundary bin when it is taken
+  // whole) go to a slot of their bin's output range [excl[d], excl[d] + n_d);
+  // otherwise the boundary bin's keys become candidates.
+  for (int i = gtid; i < nb; i += T) {
+    const uint32_t kv = keys[i];
+    const uint32_t d = nw_bin(kv, A);
+    if (d < bdig || (d == bdig && take_bin)) {
+      const uint32_t slot = excl[d] + atomicSub(&hist[d], 1u) - 1u;
+      sel[slot] = win_key(kv, i);
+      sel_bin[slot] = d;
+    } else if (d == bdig) {
+      cand[atomicAdd(&sh.n_cand, 1u)] = win_key(kv, i);
+    }
+  }
+  group_sync<T>(bar_id);
+  // Order inside each winner's bin (bins hold a few keys), P threads per
+  // winner; then the boundary bin's candidates by rank.
+  const int n_win = static_cast<int>(take_bin ? static_cast<uint32_t>(k) : above);
+  int P = 1;
+  while (P < 32 && 2 * P * n_win <= T) P <<= 1;
+  for (int b0 = 0; b0 < n_win * P; b0 += T) {
+    const int t = b0 + gtid, e = t / P, sub = t & (P - 1);
+    const bool valid = e < n_win;
+    uint64_t me = 0;
+    uint32_t lo = 0, r = 0;
+    if (valid) {
+      me = sel[e];
+      const uint32_t d = sel_bin[e];
+      lo = excl[d];
+      const uint32_t hi = d == bdig ? static_cast<uint32_t>(k) : excl[d + 1];
+      for (uint32_t i = lo + sub; i < hi; i += P) r += sel[i] > me ? 1u : 0u;
+    }
+    for (int o = 1; o < P; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
+    if (valid && sub == 0) out[lo + r] = static_cast<int32_t>(~static_cast<uint32_t>(me));
+  }
+  if (!take_bin) {
+    const int n_c = static_cast<int>(cnt);
+    for (int e = gtid; e < n_c; e += T) {
+      const uint64_t me = cand[e];
+      uint32_t r = 0;
+      for (int i = 0; i < n_c; ++i) r += cand[i] > me ? 1u : 0u;
+      if (r < need) out[above + r] = static_cast<int32_t>(~static_cast<uint32_t>(me));
+    }
+  }
+  return true;
+}
+
 }  // namespace qsa

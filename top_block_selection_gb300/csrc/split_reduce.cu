@@ -446,6 +446,7 @@ cudaError_t launch_split_reduce(const SplitReduceProblem& p, const DeviceInfo& d
   a.count = a.S > 1 ? reinterpret_cast<uint32_t*>(ws) : nullptr;
   a.part_sum = a.S > 1 ? reinterpret_cast<float*>(ws + counters) : nullptr;
   a.part_out = a.S > 1 ? reinterpret_cast<float*>(ws + counters + sums) : nullptr;
+  plan_add("split_reduce_kernel");
   return launch_pdl(split_reduce_kernel,
                     dim3(static_cast<unsigned>(a.S), static_cast<unsigned>(a.RS),
                          static_cast<unsigned>(p.G)),
