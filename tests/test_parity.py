@@ -191,15 +191,15 @@ def test_large_step_paths_agree(tbs):
 
 def test_arm_reports_the_plan_that_ran(tbs):
     """qsa_arm() names the kernels the last call on this thread launched: the
-    one-tile-per-CTA step kernel for the 128K step, the 8-CTA fused kernel
-    for a batched launch, and the chain of separate kernels for a step too
-    large for either fused form; qsa_select_step_launches agrees."""
+    8-CTA fused kernel for the 128K step and for a batched launch, and the
+    chain of separate kernels for a step too large for the fused launch;
+    qsa_select_step_launches agrees."""
     h = qi.BY_NAME["long128k_nq256_h8_d128_kv131072"]
     q32, _ = qi.make_f32_inputs(h)
     _, kb = qi.make_inputs(h)
     tbs.qsa_select_step(dev(q32), dev(kb), h.n_kv, h.k, h.block)
     arm = tbs.qsa_arm()
-    assert "last call on this thread: 1 launch: select_step_kernel" in arm, arm
+    assert "last call on this thread: 1 launch: fused_step_kernel" in arm, arm
     assert tbs.qsa_select_step_launches(h.nq, h.H, h.D, h.n_kv, h.k, h.block, with_q16=False) == 1
     tbs.qsa_select_step_batched(dev(q32[None]), dev(kb), h.n_kv, h.k, h.block)
     assert "1 launch: fused_step_kernel" in tbs.qsa_arm()

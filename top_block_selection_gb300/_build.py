@@ -21,7 +21,7 @@ LIBDIR = os.path.join(HERE, "lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIBPATH = os.path.join(LIBDIR, "libqsa.so")
 
-SOURCES = ["qsa_runtime.cu", "score_tc.cu", "select.cu", "convert.cu", "fused.cu", "step.cu", "split_reduce.cu",
+SOURCES = ["qsa_runtime.cu", "score_tc.cu", "select.cu", "convert.cu", "fused.cu", "split_reduce.cu",
            "split_reduce_static.cu", "qsa_api.cpp"]
 HEADERS = ["qsa_device.cuh", "qsa_internal.h", "select_row.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

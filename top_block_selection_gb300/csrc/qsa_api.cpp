@@ -206,12 +206,10 @@ qsa_status qsa_score_select(const uint16_t* q, const uint16_t* kb, int32_t nq, i
   if (g.nb > 0 && (!q || !kb)) return QSA_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
-  qsa::FusedProblem p{nullptr, q,       nullptr,  kb, scores, ids, nq, H, D, g.nb, g.n_full,
-                      g.has_tail, k, 1, 0};
-  if (g.nb > 0 && qsa::step_supported(nq, H, D, g.nb, g.n_full, k, *dev))
-    return from_cuda(qsa::launch_step(p, *dev, as_cuda(stream)));
   if (g.nb > 0 && use_separate(nq, H, *dev))
     return run_separate(q, kb, nq, H, D, g, k, scores, ids, *dev, as_cuda(stream));
+  qsa::FusedProblem p{nullptr, q,       nullptr,  kb, scores, ids, nq, H, D, g.nb, g.n_full,
+                      g.has_tail, k, 1, 0};
   return from_cuda(qsa::launch_fused(p, *dev, as_cuda(stream)));
 }
 
@@ -229,11 +227,6 @@ qsa_status qsa_select_step(const float* q32, uint16_t* q16, const uint16_t* kb, 
   if (!aligned(q32, 16) || !aligned(q16, 16)) return QSA_ERR_MISALIGNED;
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
-  if (g.nb > 0 && qsa::step_supported(nq, H, D, g.nb, g.n_full, k, *dev)) {
-    qsa::FusedProblem p{q32, nullptr, q16, kb, scores, ids, nq, H, D, g.nb, g.n_full,
-                        g.has_tail, k, 1, 0};
-    return from_cuda(qsa::launch_step(p, *dev, as_cuda(stream)));
-  }
   if (q16 && g.nb > 0 && use_separate(nq, H, *dev)) {
     cudaStream_t s = as_cuda(stream);
     const int64_t n = static_cast<int64_t>(nq) * H * D;
@@ -254,7 +247,6 @@ int32_t qsa_select_step_launches(int32_t nq, int32_t H, int32_t D, int64_t n_kv,
   if (nq == 0 || nb == 0) return 0;
   const DeviceInfo* dev = nullptr;
   if (device_or_error(&dev, false) != QSA_OK) return -1;
-  if (qsa::step_supported(nq, H, D, nb, n_kv / block, k, *dev)) return 1;
   if (!with_q16 || !use_separate(nq, H, *dev)) return 1;
   // convert (nq * H * D is a multiple of 8: one vector launch), the score
   // kernel when there are full blocks, the tail kernel when there is a tail,

@@ -98,14 +98,6 @@ cudaError_t init_fused_kernels(const DeviceInfo& dev);
 int64_t fused_blocks(int32_t nq, int32_t H, const DeviceInfo& dev);
 cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStream_t stream);
 
-// The one-tile-per-CTA step kernel (step.cu): single-batch steps whose
-// blocks fit one 16-CTA cluster per query group and whose rows' keys fit the
-// dead query tile. step_supported says whether it takes a problem.
-cudaError_t init_step_kernels(const DeviceInfo& dev);
-bool step_supported(int32_t nq, int32_t H, int32_t D, int64_t nb, int64_t n_full, int32_t k,
-                    const DeviceInfo& dev);
-cudaError_t launch_step(const FusedProblem& p, const DeviceInfo& dev, cudaStream_t stream);
-
 cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k, int32_t* ids,
                           const DeviceInfo& dev, cudaStream_t stream);
 

@@ -45,7 +45,7 @@ const DeviceInfo* current_device(cudaError_t* err) {
     }
     d.status_word = static_cast<uint32_t*>(p);
     if ((e = init_score_kernels(d)) != cudaSuccess || (e = init_select_kernels(d)) != cudaSuccess ||
-        (e = init_fused_kernels(d)) != cudaSuccess || (e = init_step_kernels(d)) != cudaSuccess || (e = init_split_reduce_kernel(d)) != cudaSuccess) {
+        (e = init_fused_kernels(d)) != cudaSuccess || (e = init_split_reduce_kernel(d)) != cudaSuccess) {
       *err = e;
       return nullptr;
     }

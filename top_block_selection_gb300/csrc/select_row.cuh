@@ -807,145 +807,196 @@ __device__ void select_row_g(const uint32_t* keys, int nb, int k, int32_t* __res
 }
 
 
-// ------------------------------------- narrow window select, keys in smem
-// The top-k of one row whose keys[0..nb) are in shared memory, by a group of
-// T threads (whole warps), with a first digit of kSelNwBins bins of 1/64
-// octave measured down from an anchor A: the largest key other than
-// keys[skip] (skip < 0: the largest key). bin(key) = 0 for key >= A,
-// otherwise (A - key) >> kSelWinShift; bins from kSelNwBins down are below
-// the window and not counted. Keys above A (at most keys[skip]) share bin 0
-// with the keys just below A; every bin is ordered by the full key, so the
-// result does not depend on the anchor: only whether the window holds the
-// k-th largest key does. One warp scans the bins. Dense score rows put the
-// k-th key within a few octaves of the top, in a bin of a few keys: the
-// search ends after one histogram. Otherwise (the k-th key below the window,
-// more than kSelBinMax keys in its bin, or k >= nb) the function returns
-// false having written only scratch, and the caller runs select_row_g.
-// Scratch: hist >= 2 * kSelNwBins words (16-byte aligned), cand kSelBinMax,
-// sel and sel_bin k each. Ends without a barrier after the last read of
-// scratch; the caller synchronises before reusing it.
-constexpr int kSelNwBins = 256;
+// ------------------------- threshold select, keys in smem, no atomics
+// The top-k of one row whose keys[0..nb) are in shared memory (16-byte
+// aligned, padded to a multiple of 4 keys), by a group of T threads (whole
+// warps). Thread t holds the keys of 16-byte chunks [t*C4, (t+1)*C4) in
+// registers (C4 <= C, else the function declines).
+//   1. A lower bound L on the k-th largest key: the row is cut into segments
+//      of sg adjacent threads' keys (sg the widest power of two <= 32 still
+//      giving at least k non-empty segments); each segment's largest key is
+//      an element, so at least k keys are >= L = the smallest segment
+//      maximum (L = 0 when the row has fewer than k segments). M, the
+//      largest key other than keys[skip], anchors the thresholds of step 3.
+//   2. The keys >= L (typically an eighth of the row) are compacted into
+//      list A by one group-wide prefix scan, as 64-bit keys (key << 32 |
+//      ~index: distinct, larger means earlier in the output).
+//   3. Eight thresholds spread over [L, M]: each thread counts its list-A
+//      entries at or above each (16-bit fields packed two to a word, added
+//      over the warp by redux); t* = the highest threshold reached by k.
+//   4. The entries >= t* (k plus a few dozen) are compacted into list B.
+//   5. Each list-B entry's output slot is its rank in list B.
+// No shared-memory atomics, and the per-key work is two compares: the rest
+// runs on the short lists. Returns false having written only scratch (k >=
+// nb, C4 > C, or more than kSelThrCandMax entries in list A); the caller then
+// runs select_row_g. Scratch: cand 2 * kSelThrCandMax 64-bit words. Ends
+// without a barrier after the last read of scratch; the caller synchronises
+// before reusing it.
+constexpr int kSelThrCandMax = 512;
+constexpr int kSelThr = 8;
 
-struct NwShared {
-  uint32_t wmax[8];
-  uint32_t bdig, above, cnt, n_cand, ok;
+struct ThrShared {
+  uint32_t wmax[8], wmin[8], wseg[8], woff[8], woff2[8];
+  uint32_t wcnt[8][kSelThr / 2];
 };
 
-__device__ __forceinline__ uint32_t nw_bin(uint32_t key, uint32_t anchor) {
-  return key >= anchor ? 0u : (anchor - key) >> kSelWinShift;
+// Exclusive prefix of v over the group (warp scan, then the warp totals in
+// sh_w after a barrier); *total gets the group's sum.
+template <int T>
+__device__ __forceinline__ uint32_t thr_scan(uint32_t v, uint32_t* sh_w, uint32_t* total,
+                                             int gtid, int bar_id) {
+  constexpr int kW = T / 32;
+  const int lane = gtid & 31, gw = gtid >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  if (lane == 31) sh_w[gw] = incl;
+  group_sync<T>(bar_id);
+  uint32_t before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) {
+    const uint32_t x = sh_w[w];
+    before += w < gw ? x : 0u;
+    tot += x;
+  }
+  *total = tot;
+  return before + incl - v;
 }
 
-template <int T>
-__device__ bool select_row_narrow(const uint32_t* keys, int nb, int k, int skip,
-                                  int32_t* __restrict__ out, uint32_t* hist, uint64_t* cand,
-                                  uint64_t* sel, uint32_t* sel_bin, NwShared& sh, int gtid,
-                                  int bar_id) {
+template <int T, int C>
+__device__ bool select_row_thr(const uint32_t* keys, int nb, int k, int skip,
+                               int32_t* __restrict__ out, uint64_t* cand, ThrShared& sh, int gtid,
+                               int bar_id) {
   constexpr int kW = T / 32;
   static_assert(kW >= 1 && kW <= 8, "1 to 8 warps per row");
-  const int lane = gtid & 31;
+  const int lane = gtid & 31, gw = gtid >> 5;
   if (k >= nb) return false;
-  uint32_t* excl = hist + kSelNwBins;
-  // the anchor: the row's largest key other than keys[skip]
-  uint32_t m = 0;
-  for (int i = gtid; i < nb; i += T) {
-    const uint32_t kv = keys[i];
-    if (i != skip) m = max(m, kv);
+  const int n4 = (nb + 3) >> 2;
+  const int C4 = (n4 + T - 1) / T;
+  if (C4 > C) return false;
+  const int c_lo = gtid * C4;
+  const int nt = (n4 + C4 - 1) / C4;
+  // ---- 1: keys to registers (0 = no key), segment bound and anchor
+  uint32_t kr[4 * C];
+  const uint4* kv4 = reinterpret_cast<const uint4*>(keys);
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (c < C4 && c_lo + c < n4) v = kv4[c_lo + c];
+    kr[4 * c] = v.x;
+    kr[4 * c + 1] = v.y;
+    kr[4 * c + 2] = v.z;
+    kr[4 * c + 3] = v.w;
   }
-  m = __reduce_max_sync(0xFFFFFFFFu, m);
-  if (lane == 0) sh.wmax[gtid >> 5] = m;
-  for (int i = gtid; i < kSelNwBins; i += T) hist[i] = 0u;
-  if (gtid == 0) sh.n_cand = 0;
-  group_sync<T>(bar_id);
-  uint32_t A = 0;
+  uint32_t mx = 0, ma = 0;
 #pragma unroll
-  for (int w = 0; w < kW; ++w) A = max(A, sh.wmax[w]);
-  for (int i = gtid; i < nb; i += T) {
-    const uint32_t d = nw_bin(keys[i], A);
-    if (d < kSelNwBins) atomicAdd(&hist[d], 1u);
+  for (int j = 0; j < 4 * C; ++j) {
+    const int i = 4 * c_lo + j;
+    if (i >= nb) kr[j] = 0u;  // padding past the row
+    mx = max(mx, kr[j]);
+    ma = max(ma, i != skip ? kr[j] : 0u);
+  }
+  int sg = 32;
+  while (sg > 1 && nt / sg < k) sg >>= 1;
+  uint32_t m = mx;
+  for (int o = 1; o < sg; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  const uint32_t lo = __reduce_min_sync(0xFFFFFFFFu, m != 0u ? m : 0xFFFFFFFFu);
+  const uint32_t hi = __reduce_max_sync(0xFFFFFFFFu, ma);
+  const uint32_t nseg = __popc(__ballot_sync(0xFFFFFFFFu, (lane & (sg - 1)) == 0 && m != 0u));
+  if (lane == 0) {
+    sh.wmax[gw] = hi;
+    sh.wmin[gw] = lo;
+    sh.wseg[gw] = nseg;
   }
   group_sync<T>(bar_id);
-  if (gtid < 32) {
-    // lane l: bins [8l, 8l + 8), top (bin 0) first
-    uint32_t c[8];
-    const uint4 v0 = *reinterpret_cast<const uint4*>(hist + 8 * lane);
-    const uint4 v1 = *reinterpret_cast<const uint4*>(hist + 8 * lane + 4);
-    c[0] = v0.x; c[1] = v0.y; c[2] = v0.z; c[3] = v0.w;
-    c[4] = v1.x; c[5] = v1.y; c[6] = v1.z; c[7] = v1.w;
-    uint32_t local = 0;
+  uint32_t M = 0, L = 0xFFFFFFFFu, S = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) local += c[j];
-    uint32_t incl = local;
+  for (int w = 0; w < kW; ++w) {
+    M = max(M, sh.wmax[w]);
+    L = min(L, sh.wmin[w]);
+    S += sh.wseg[w];
+  }
+  if (S < static_cast<uint32_t>(k)) L = 1;  // every key (key 0 is no key)
+  L = min(max(L, 1u), max(M, 1u));
+  // ---- 2: list A = the keys >= L
+  uint32_t mine = 0;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-      if (lane >= off) incl += t;
+  for (int j = 0; j < 4 * C; ++j) mine += kr[j] >= L ? 1u : 0u;
+  uint32_t n_a;
+  uint32_t pos = thr_scan<T>(mine, sh.woff, &n_a, gtid, bar_id);
+  if (n_a > static_cast<uint32_t>(kSelThrCandMax)) return false;
+  uint64_t* la = cand;
+  uint64_t* lb = cand + kSelThrCandMax;
+  if (mine) {
+#pragma unroll
+    for (int j = 0; j < 4 * C; ++j)
+      if (kr[j] >= L) la[pos++] = win_key(kr[j], 4 * c_lo + j);
+  }
+  group_sync<T>(bar_id);
+  // ---- 3: counts of list A at eight thresholds L + (j + 1) * step
+  const uint32_t step = (M - L) / (kSelThr + 1);
+  const int na = static_cast<int>(n_a);
+  uint32_t pc[kSelThr / 2] = {0u, 0u, 0u, 0u};
+  for (int e = gtid; e < na; e += T) {
+    const uint32_t kv = static_cast<uint32_t>(la[e] >> 32);
+#pragma unroll
+    for (int j = 0; j < kSelThr; ++j)
+      pc[j >> 1] += (kv >= L + (j + 1) * step ? 1u : 0u) << ((j & 1) * 16);
+  }
+#pragma unroll
+  for (int w = 0; w < kSelThr / 2; ++w) pc[w] = __reduce_add_sync(0xFFFFFFFFu, pc[w]);
+  if (lane == 0) {
+#pragma unroll
+    for (int w = 0; w < kSelThr / 2; ++w) sh.wcnt[gw][w] = pc[w];
+  }
+  group_sync<T>(bar_id);
+  uint32_t thr = L;
+#pragma unroll
+  for (int j = 0; j < kSelThr; ++j) {
+    uint32_t cj = 0;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) cj += (sh.wcnt[w][j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
+    if (cj >= static_cast<uint32_t>(k)) thr = L + (j + 1) * step;
+  }
+  // ---- 4: list B = the list-A entries >= t*
+  constexpr int kPer = (kSelThrCandMax + T - 1) / T;
+  uint64_t own[kPer];
+  uint32_t mine_b = 0;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int e = gtid + q * T;
+    own[q] = e < na ? la[e] : 0ull;
+    mine_b += (e < na && static_cast<uint32_t>(own[q] >> 32) >= thr) ? 1u : 0u;
+  }
+  uint32_t n_b;
+  uint32_t pb = thr_scan<T>(mine_b, sh.woff2, &n_b, gtid, bar_id);
+  if (mine_b) {
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int e = gtid + q * T;
+      if (e < na && static_cast<uint32_t>(own[q] >> 32) >= thr) lb[pb++] = own[q];
     }
-    const uint32_t kk = static_cast<uint32_t>(k);
-    uint32_t run = incl - local;
-    uint32_t e[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      e[j] = run;
-      if (run < kk && kk <= run + c[j]) {
-        sh.bdig = static_cast<uint32_t>(8 * lane + j);
-        sh.above = run;
-        sh.cnt = c[j];
-      }
-      run += c[j];
-    }
-    *reinterpret_cast<uint4*>(excl + 8 * lane) = make_uint4(e[0], e[1], e[2], e[3]);
-    *reinterpret_cast<uint4*>(excl + 8 * lane + 4) = make_uint4(e[4], e[5], e[6], e[7]);
-    if (lane == 31) sh.ok = incl >= kk ? 1u : 0u;
   }
   group_sync<T>(bar_id);
-  if (!sh.ok) return false;  // the k-th key lies below the window
-  const uint32_t bdig = sh.bdig, above = sh.above, cnt = sh.cnt;
-  const uint32_t need = static_cast<uint32_t>(k) - above;
-  const bool take_bin = cnt == need;
-  if (!take_bin && cnt > static_cast<uint32_t>(kSelBinMax)) return false;
-  // Winners (bins above the boundary, and the boundary bin when it is taken
-  // whole) go to a slot of their bin's output range [excl[d], excl[d] + n_d);
-  // otherwise the boundary bin's keys become candidates.
-  for (int i = gtid; i < nb; i += T) {
-    const uint32_t kv = keys[i];
-    const uint32_t d = nw_bin(kv, A);
-    if (d < bdig || (d == bdig && take_bin)) {
-      const uint32_t slot = excl[d] + atomicSub(&hist[d], 1u) - 1u;
-      sel[slot] = win_key(kv, i);
-      sel_bin[slot] = d;
-    } else if (d == bdig) {
-      cand[atomicAdd(&sh.n_cand, 1u)] = win_key(kv, i);
-    }
-  }
-  group_sync<T>(bar_id);
-  // Order inside each winner's bin (bins hold a few keys), P threads per
-  // winner; then the boundary bin's candidates by rank.
-  const int n_win = static_cast<int>(take_bin ? static_cast<uint32_t>(k) : above);
+  // ---- 5: output slot = rank in list B (P threads per entry)
+  const int nbb = static_cast<int>(n_b);
   int P = 1;
-  while (P < 32 && 2 * P * n_win <= T) P <<= 1;
-  for (int b0 = 0; b0 < n_win * P; b0 += T) {
-    const int t = b0 + gtid, e = t / P, sub = t & (P - 1);
-    const bool valid = e < n_win;
-    uint64_t me = 0;
-    uint32_t lo = 0, r = 0;
+  while (P < 32 && 2 * P * nbb <= T) P <<= 1;
+  for (int b0 = 0; b0 < nbb * P; b0 += T) {
+    const int tt = b0 + gtid, e = tt / P, sub = tt & (P - 1);
+    const bool valid = e < nbb;
+    const uint64_t me = valid ? lb[e] : 0ull;
+    uint32_t r = 0;
     if (valid) {
-      me = sel[e];
-      const uint32_t d = sel_bin[e];
-      lo = excl[d];
-      const uint32_t hi = d == bdig ? static_cast<uint32_t>(k) : excl[d + 1];
-      for (uint32_t i = lo + sub; i < hi; i += P) r += sel[i] > me ? 1u : 0u;
+#pragma unroll 4
+      for (int i = sub; i < nbb; i += P) r += lb[i] > me ? 1u : 0u;
     }
     for (int o = 1; o < P; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
-    if (valid && sub == 0) out[lo + r] = static_cast<int32_t>(~static_cast<uint32_t>(me));
-  }
-  if (!take_bin) {
-    const int n_c = static_cast<int>(cnt);
-    for (int e = gtid; e < n_c; e += T) {
-      const uint64_t me = cand[e];
-      uint32_t r = 0;
-      for (int i = 0; i < n_c; ++i) r += cand[i] > me ? 1u : 0u;
-      if (r < need) out[above + r] = static_cast<int32_t>(~static_cast<uint32_t>(me));
-    }
+    if (valid && sub == 0 && r < static_cast<uint32_t>(k))
+      out[r] = static_cast<int32_t>(~static_cast<uint32_t>(me));
   }
   return true;
 }
