@@ -807,198 +807,4 @@ __device__ void select_row_g(const uint32_t* keys, int nb, int k, int32_t* __res
 }
 
 
-// ------------------------- threshold select, keys in smem, no atomics
-// The top-k of one row whose keys[0..nb) are in shared memory (16-byte
-// aligned, padded to a multiple of 4 keys), by a group of T threads (whole
-// warps). Thread t holds the keys of 16-byte chunks [t*C4, (t+1)*C4) in
-// registers (C4 <= C, else the function declines).
-//   1. A lower bound L on the k-th largest key: the row is cut into segments
-//      of sg adjacent threads' keys (sg the widest power of two <= 32 still
-//      giving at least k non-empty segments); each segment's largest key is
-//      an element, so at least k keys are >= L = the smallest segment
-//      maximum (L = 0 when the row has fewer than k segments). M, the
-//      largest key other than keys[skip], anchors the thresholds of step 3.
-//   2. The keys >= L (typically an eighth of the row) are compacted into
-//      list A by one group-wide prefix scan, as 64-bit keys (key << 32 |
-//      ~index: distinct, larger means earlier in the output).
-//   3. Eight thresholds spread over [L, M]: each thread counts its list-A
-//      entries at or above each (16-bit fields packed two to a word, added
-//      over the warp by redux); t* = the highest threshold reached by k.
-//   4. The entries >= t* (k plus a few dozen) are compacted into list B.
-//   5. Each list-B entry's output slot is its rank in list B.
-// No shared-memory atomics, and the per-key work is two compares: the rest
-// runs on the short lists. Returns false having written only scratch (k >=
-// nb, C4 > C, or more than kSelThrCandMax entries in list A); the caller then
-// runs select_row_g. Scratch: cand 2 * kSelThrCandMax 64-bit words. Ends
-// without a barrier after the last read of scratch; the caller synchronises
-// before reusing it.
-constexpr int kSelThrCandMax = 512;
-constexpr int kSelThr = 8;
-
-struct ThrShared {
-  uint32_t wmax[8], wmin[8], wseg[8], woff[8], woff2[8];
-  uint32_t wcnt[8][kSelThr / 2];
-};
-
-// Exclusive prefix of v over the group (warp scan, then the warp totals in
-// sh_w after a barrier); *total gets the group's sum.
-template <int T>
-__device__ __forceinline__ uint32_t thr_scan(uint32_t v, uint32_t* sh_w, uint32_t* total,
-                                             int gtid, int bar_id) {
-  constexpr int kW = T / 32;
-  const int lane = gtid & 31, gw = gtid >> 5;
-  uint32_t incl = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-    if (lane >= off) incl += t;
-  }
-  if (lane == 31) sh_w[gw] = incl;
-  group_sync<T>(bar_id);
-  uint32_t before = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < kW; ++w) {
-    const uint32_t x = sh_w[w];
-    before += w < gw ? x : 0u;
-    tot += x;
-  }
-  *total = tot;
-  return before + incl - v;
-}
-
-template <int T, int C>
-__device__ bool select_row_thr(const uint32_t* keys, int nb, int k, int skip,
-                               int32_t* __restrict__ out, uint64_t* cand, ThrShared& sh, int gtid,
-                               int bar_id) {
-  constexpr int kW = T / 32;
-  static_assert(kW >= 1 && kW <= 8, "1 to 8 warps per row");
-  const int lane = gtid & 31, gw = gtid >> 5;
-  if (k >= nb) return false;
-  const int n4 = (nb + 3) >> 2;
-  const int C4 = (n4 + T - 1) / T;
-  if (C4 > C) return false;
-  const int c_lo = gtid * C4;
-  const int nt = (n4 + C4 - 1) / C4;
-  // ---- 1: keys to registers (0 = no key), segment bound and anchor
-  uint32_t kr[4 * C];
-  const uint4* kv4 = reinterpret_cast<const uint4*>(keys);
-#pragma unroll
-  for (int c = 0; c < C; ++c) {
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (c < C4 && c_lo + c < n4) v = kv4[c_lo + c];
-    kr[4 * c] = v.x;
-    kr[4 * c + 1] = v.y;
-    kr[4 * c + 2] = v.z;
-    kr[4 * c + 3] = v.w;
-  }
-  uint32_t mx = 0, ma = 0;
-#pragma unroll
-  for (int j = 0; j < 4 * C; ++j) {
-    const int i = 4 * c_lo + j;
-    if (i >= nb) kr[j] = 0u;  // padding past the row
-    mx = max(mx, kr[j]);
-    ma = max(ma, i != skip ? kr[j] : 0u);
-  }
-  int sg = 32;
-  while (sg > 1 && nt / sg < k) sg >>= 1;
-  uint32_t m = mx;
-  for (int o = 1; o < sg; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  const uint32_t lo = __reduce_min_sync(0xFFFFFFFFu, m != 0u ? m : 0xFFFFFFFFu);
-  const uint32_t hi = __reduce_max_sync(0xFFFFFFFFu, ma);
-  const uint32_t nseg = __popc(__ballot_sync(0xFFFFFFFFu, (lane & (sg - 1)) == 0 && m != 0u));
-  if (lane == 0) {
-    sh.wmax[gw] = hi;
-    sh.wmin[gw] = lo;
-    sh.wseg[gw] = nseg;
-  }
-  group_sync<T>(bar_id);
-  uint32_t M = 0, L = 0xFFFFFFFFu, S = 0;
-#pragma unroll
-  for (int w = 0; w < kW; ++w) {
-    M = max(M, sh.wmax[w]);
-    L = min(L, sh.wmin[w]);
-    S += sh.wseg[w];
-  }
-  if (S < static_cast<uint32_t>(k)) L = 1;  // every key (key 0 is no key)
-  L = min(max(L, 1u), max(M, 1u));
-  // ---- 2: list A = the keys >= L
-  uint32_t mine = 0;
-#pragma unroll
-  for (int j = 0; j < 4 * C; ++j) mine += kr[j] >= L ? 1u : 0u;
-  uint32_t n_a;
-  uint32_t pos = thr_scan<T>(mine, sh.woff, &n_a, gtid, bar_id);
-  if (n_a > static_cast<uint32_t>(kSelThrCandMax)) return false;
-  uint64_t* la = cand;
-  uint64_t* lb = cand + kSelThrCandMax;
-  if (mine) {
-#pragma unroll
-    for (int j = 0; j < 4 * C; ++j)
-      if (kr[j] >= L) la[pos++] = win_key(kr[j], 4 * c_lo + j);
-  }
-  group_sync<T>(bar_id);
-  // ---- 3: counts of list A at eight thresholds L + (j + 1) * step
-  const uint32_t step = (M - L) / (kSelThr + 1);
-  const int na = static_cast<int>(n_a);
-  uint32_t pc[kSelThr / 2] = {0u, 0u, 0u, 0u};
-  for (int e = gtid; e < na; e += T) {
-    const uint32_t kv = static_cast<uint32_t>(la[e] >> 32);
-#pragma unroll
-    for (int j = 0; j < kSelThr; ++j)
-      pc[j >> 1] += (kv >= L + (j + 1) * step ? 1u : 0u) << ((j & 1) * 16);
-  }
-#pragma unroll
-  for (int w = 0; w < kSelThr / 2; ++w) pc[w] = __reduce_add_sync(0xFFFFFFFFu, pc[w]);
-  if (lane == 0) {
-#pragma unroll
-    for (int w = 0; w < kSelThr / 2; ++w) sh.wcnt[gw][w] = pc[w];
-  }
-  group_sync<T>(bar_id);
-  uint32_t thr = L;
-#pragma unroll
-  for (int j = 0; j < kSelThr; ++j) {
-    uint32_t cj = 0;
-#pragma unroll
-    for (int w = 0; w < kW; ++w) cj += (sh.wcnt[w][j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
-    if (cj >= static_cast<uint32_t>(k)) thr = L + (j + 1) * step;
-  }
-  // ---- 4: list B = the list-A entries >= t*
-  constexpr int kPer = (kSelThrCandMax + T - 1) / T;
-  uint64_t own[kPer];
-  uint32_t mine_b = 0;
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int e = gtid + q * T;
-    own[q] = e < na ? la[e] : 0ull;
-    mine_b += (e < na && static_cast<uint32_t>(own[q] >> 32) >= thr) ? 1u : 0u;
-  }
-  uint32_t n_b;
-  uint32_t pb = thr_scan<T>(mine_b, sh.woff2, &n_b, gtid, bar_id);
-  if (mine_b) {
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      const int e = gtid + q * T;
-      if (e < na && static_cast<uint32_t>(own[q] >> 32) >= thr) lb[pb++] = own[q];
-    }
-  }
-  group_sync<T>(bar_id);
-  // ---- 5: output slot = rank in list B (P threads per entry)
-  const int nbb = static_cast<int>(n_b);
-  int P = 1;
-  while (P < 32 && 2 * P * nbb <= T) P <<= 1;
-  for (int b0 = 0; b0 < nbb * P; b0 += T) {
-    const int tt = b0 + gtid, e = tt / P, sub = tt & (P - 1);
-    const bool valid = e < nbb;
-    const uint64_t me = valid ? lb[e] : 0ull;
-    uint32_t r = 0;
-    if (valid) {
-#pragma unroll 4
-      for (int i = sub; i < nbb; i += P) r += lb[i] > me ? 1u : 0u;
-    }
-    for (int o = 1; o < P; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
-    if (valid && sub == 0 && r < static_cast<uint32_t>(k))
-      out[r] = static_cast<int32_t>(~static_cast<uint32_t>(me));
-  }
-  return true;
-}
-
 }  // namespace qsa
