@@ -70,8 +70,11 @@ inline size_t select_window_bytes(int32_t k) {
          ((static_cast<size_t>(k) + 3) & ~static_cast<size_t>(3)) * sizeof(uint32_t);
 }
 
+// Three CTAs per SM (at most 85 registers a thread): the select is bound by
+// the latency of its barrier-separated phases, so more rows in flight per SM
+// raise the throughput of many-row launches.
 template <int R>
-__global__ void __launch_bounds__(kWinThreads)
+__global__ void __launch_bounds__(kWinThreads, 3)
     select_window_kernel(const float* __restrict__ scores, int32_t nb, int32_t k,
                          int32_t* __restrict__ ids) {
   extern __shared__ __align__(16) uint8_t sm_raw[];

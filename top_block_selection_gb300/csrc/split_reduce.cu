@@ -27,6 +27,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
@@ -383,6 +384,216 @@ __global__ void __launch_bounds__(kSrThreads) split_reduce_kernel(const SrArgs a
   }
 }
 
+// ------------------------------------ cluster form: one cluster per row
+// One thread-block cluster of cs CTAs per (group, row); CTA rank q reduces the
+// chunks [q*cpc, (q+1)*cpc) of 128 blocks: it bulk-copies each chunk's fp16
+// partial outputs (whole rows of C channels, one contiguous copy per chunk)
+// into shared memory and finds the maximum of its blocks' partial_max; each
+// CTA stores its maximum into every CTA's shared memory (distributed shared
+// memory), so after one cluster barrier every CTA has the row's maximum. It
+// then forms its chunks' partials in the fixed order (runs of 32 blocks
+// accumulated block by block, a chunk's runs added in order) and stores them
+// into CTA rank 0's shared memory; after a second cluster barrier rank 0
+// adds them in chunk order and divides. Every exchange is a store into the
+// reader's shared memory, so no CTA waits on a remote load. The arithmetic is the row-split kernel's,
+// operation for operation: the same bits, with no workspace, no arrival
+// counter and no global round trip. Only a few bytes per chunk cross between
+// CTAs (distributed shared memory moves bulk data slowly).
+constexpr int kScThreads = 256;
+constexpr int kScMaxCpc = 4;    // chunks per CTA at most
+constexpr int kScMaxCs = 8;     // CTAs per cluster at most (portable)
+
+struct ScArgs {
+  const float* pm;     // [G][R][B]
+  const float* ps;     // [G][R][B]
+  const __half* po;    // [G][R][B][C]
+  float* out;          // [G][R][C]
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int R, B, C, cs, cpc;
+};
+
+__device__ __forceinline__ uint32_t sc_cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void sc_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Stores v at the same shared-memory offset as `local` in CTA `rank` of the
+// cluster (a plain weak store; the next cluster barrier makes it visible).
+__device__ __forceinline__ void sc_st_peer(float* local, uint32_t rank, float v) {
+  uint32_t addr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(kScThreads)
+    split_cluster_kernel(const ScArgs a) {
+  extern __shared__ __align__(128) uint8_t sc_stage[];  // [cpc][128][C] fp16, then floats
+  __shared__ __align__(8) uint64_t bar_chunk[kScMaxCpc];
+  __shared__ float s_red[kScThreads / 32];
+  __shared__ float s_lmax[kScMaxCs];  // every CTA's maximum, pushed by its owner
+  __shared__ int s_ok;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int R = a.R, B = a.B, C = a.C, cpc = a.cpc, cs = a.cs;
+  const int q = static_cast<int>(sc_cluster_rank());
+  const int row_id = blockIdx.x / cs;  // (group, row)
+  const int64_t row = row_id;
+  const int n_chunks = (B + kSrChunk - 1) / kSrChunk;
+  const int j0 = q * cpc, j1 = min(n_chunks, j0 + cpc);  // this CTA's chunks
+  const int b_lo = j0 * kSrChunk, b_hi = min(B, j1 * kSrChunk);
+  const size_t chunk_halves = static_cast<size_t>(kSrChunk) * C;
+  float* s_scale = reinterpret_cast<float*>(sc_stage + static_cast<size_t>(cpc) * chunk_halves * 2);
+  float* s_psum = s_scale + cpc * kSrChunk;
+  float* run_out = s_psum + cpc * kSrChunk;                       // [cpc][kSrRuns][C]
+  float* run_sum = run_out + static_cast<size_t>(cpc) * kSrRuns * C;  // [cpc][kSrRuns]
+  float* gather = run_sum + cpc * kSrRuns;  // rank 0: [n_chunks][C + 1], pushed by the owners
+  const __half* stage = reinterpret_cast<const __half*>(sc_stage);
+  (void)R;
+
+  pdl_launch_dependents();
+  if (tid == 0) {
+    for (int i = 0; i < kScMaxCpc; ++i) mbar_init(&bar_chunk[i], 1);
+    fence_mbarrier_init();
+    s_ok = 1;
+    // this CTA's inputs on their way to L2 while the previous kernel
+    // finishes (hints: they change no value a later load observes)
+    bulk_prefetch_l2(a.po + (row * B + b_lo) * C, static_cast<uint32_t>(b_hi - b_lo) * C * 2u);
+    const uint32_t pbytes = (static_cast<uint32_t>(b_hi - b_lo) * 4u) & ~15u;
+    if (((row * B + b_lo) & 3) == 0 && pbytes) {
+      bulk_prefetch_l2(a.pm + row * B + b_lo, pbytes);
+      bulk_prefetch_l2(a.ps + row * B + b_lo, pbytes);
+    }
+  }
+  __syncthreads();
+  pdl_wait();
+  if (tid == 0) {
+    for (int j = j0; j < j1; ++j) {
+      const int nbk = min(kSrChunk, B - j * kSrChunk);
+      const uint32_t bytes = static_cast<uint32_t>(nbk) * C * 2u;
+      mbar_arrive_expect_tx(&bar_chunk[j - j0], bytes);
+      bulk_load(sc_stage + static_cast<size_t>(j - j0) * chunk_halves * 2,
+                a.po + (row * B + static_cast<int64_t>(j) * kSrChunk) * C, bytes, &bar_chunk[j - j0]);
+    }
+  }
+  // This CTA's blocks' partial_max and partial_sum in registers (both loads
+  // in flight together), its maximum, then the row's over the cluster.
+  const float* pmr = a.pm + row * B;
+  const float* psr = a.ps + row * B;
+  constexpr int kScPer = kScMaxCpc * kSrChunk / kScThreads;  // blocks per thread at most
+  float pmv[kScPer], psv[kScPer];
+#pragma unroll
+  for (int i = 0; i < kScPer; ++i) {
+    const int b = b_lo + tid + i * kScThreads;
+    pmv[i] = b < b_hi ? __ldg(pmr + b) : __int_as_float(0xff800000u);
+    psv[i] = b < b_hi ? __ldg(psr + b) : 0.0f;
+  }
+  float m = pmv[0];
+#pragma unroll
+  for (int i = 1; i < kScPer; ++i) m = fmaxf(m, pmv[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if (lane == 0) s_red[warp] = m;
+  __syncthreads();
+  if (tid < cs) {
+    float mm = s_red[0];
+    for (int w = 1; w < kScThreads / 32; ++w) mm = fmaxf(mm, s_red[w]);
+    sc_st_peer(&s_lmax[q], static_cast<uint32_t>(tid), mm);  // to CTA tid of the cluster
+  }
+  sc_cluster_sync();  // every CTA's maximum has reached every CTA
+  float M = s_lmax[0];
+  for (int p = 1; p < cs; ++p) M = fmaxf(M, s_lmax[p]);
+#pragma unroll
+  for (int i = 0; i < kScPer; ++i) {
+    const int b = b_lo + tid + i * kScThreads;
+    if (b < b_hi) {
+      s_scale[b - b_lo] = exp_pinned(__fsub_rn(pmv[i], M));
+      s_psum[b - b_lo] = psv[i];
+    }
+  }
+  if (tid == 0) {
+    for (int j = j0; j < j1; ++j)
+      if (!mbar_wait_bounded(&bar_chunk[j - j0], 0, a.timeout_ns)) {
+        s_ok = 0;
+        atomicOr(a.status, kErrSplitLoadTimeout);
+      }
+    if (!s_ok)
+      for (int j = j0; j < j1; ++j) mbar_wait_bounded(&bar_chunk[j - j0], 0, a.timeout_ns);
+  }
+  __syncthreads();  // chunks landed, scales staged
+  // Runs: work item = (chunk, run, quad of 4 channels); the quad at channel 0
+  // also accumulates the run's sum.
+  const int qpr = C / 4;
+  const int items = (j1 - j0) * kSrRuns * qpr;
+  if (s_ok) {
+    for (int it = tid; it < items; it += kScThreads) {
+      const int jr = it / qpr, qq = it - jr * qpr;   // jr = local chunk * kSrRuns + run
+      const int jl = jr / kSrRuns, u = jr - jl * kSrRuns;
+      const int c = qq * 4;
+      const int bc = (j0 + jl) * kSrChunk;           // first block of the chunk
+      const int bl_lo = bc + u * kSrRun, bl_hi = min(B, bl_lo + kSrRun);
+      float o0 = 0.0f, o1 = 0.0f, o2 = 0.0f, o3 = 0.0f, acc_s = 0.0f;
+      const uint2* src = reinterpret_cast<const uint2*>(stage + static_cast<size_t>(jl) * chunk_halves + c) +
+                         static_cast<size_t>(bl_lo - bc) * (C / 4);
+      const float* scl = s_scale + (bl_lo - b_lo);
+      const float* psl = s_psum + (bl_lo - b_lo);
+      auto step = [&](int i) {
+        const uint2 v = src[static_cast<size_t>(i) * (C / 4)];
+        const float sc = scl[i];
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+        const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+        o0 = __fadd_rn(o0, __fmul_rn(sc, f01.x));
+        o1 = __fadd_rn(o1, __fmul_rn(sc, f01.y));
+        o2 = __fadd_rn(o2, __fmul_rn(sc, f23.x));
+        o3 = __fadd_rn(o3, __fmul_rn(sc, f23.y));
+        if (qq == 0) acc_s = __fadd_rn(acc_s, __fmul_rn(sc, psl[i]));
+      };
+      const int len = bl_hi - bl_lo;
+      if (len == kSrRun) {
+#pragma unroll
+        for (int i = 0; i < kSrRun; ++i) step(i);  // a whole run: no loop control
+      } else {
+        for (int i = 0; i < len; ++i) step(i);
+      }
+      *reinterpret_cast<float4*>(run_out + static_cast<size_t>(jr) * C + c) = make_float4(o0, o1, o2, o3);
+      if (qq == 0) run_sum[jr] = acc_s;
+    }
+  }
+  __syncthreads();
+  // Chunk partials: a chunk's runs added in order from 0.
+  for (int x = tid; x < (j1 - j0) * (C + 1); x += kScThreads) {
+    const int jl = x / (C + 1), c = x - jl * (C + 1);
+    const int nbk = min(kSrChunk, B - (j0 + jl) * kSrChunk);
+    const int nr = (nbk + kSrRun - 1) / kSrRun;
+    float part = 0.0f;
+    for (int u = 0; u < nr; ++u)
+      part = __fadd_rn(part, c < C ? run_out[(static_cast<size_t>(jl) * kSrRuns + u) * C + c]
+                                   : run_sum[jl * kSrRuns + u]);
+    sc_st_peer(gather + static_cast<size_t>(j0 + jl) * (C + 1) + c, 0u, part);  // to rank 0
+  }
+  sc_cluster_sync();  // every chunk partial has reached rank 0
+  if (q == 0) {
+    // chunk partials in chunk order, then the division
+    for (int c = tid; c < C; c += kScThreads) {
+      float tot = 0.0f, tot_s = 0.0f;
+      for (int j = 0; j < n_chunks; ++j) {
+        tot = __fadd_rn(tot, gather[static_cast<size_t>(j) * (C + 1) + c]);
+        tot_s = __fadd_rn(tot_s, gather[static_cast<size_t>(j) * (C + 1) + C]);
+      }
+      a.out[row * C + c] = __fdiv_rn(tot, tot_s);
+    }
+  }
+}
+
+size_t split_cluster_smem(int C, int cpc, int n_chunks) {
+  return static_cast<size_t>(cpc) * kSrChunk * C * 2 + 2 * static_cast<size_t>(cpc) * kSrChunk * 4 +
+         static_cast<size_t>(cpc) * kSrRuns * C * 4 + static_cast<size_t>(cpc) * kSrRuns * 4 +
+         static_cast<size_t>(n_chunks) * (C + 1) * 4 + 16;
+}
+
 // Rows per CTA: the whole chunk of a CTA's rows must fit one staging buffer,
 // and the grid should cover the GPU about twice.
 void split_rows(int32_t G, int32_t R, int32_t B, int32_t C, int sm_count, int* RS, int* Rs) {
@@ -407,14 +618,62 @@ size_t split_reduce_workspace_bytes(int32_t G, int32_t R, int32_t B, int32_t C) 
 }
 
 cudaError_t init_split_reduce_kernel(const DeviceInfo& dev) {
-  (void)dev;
-  return cudaFuncSetAttribute(split_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSrSmemMax);
+  cudaError_t e = cudaFuncSetAttribute(split_reduce_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSrSmemMax);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(&split_cluster_kernel))) !=
+      cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(split_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              dev.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
 }
 
 cudaError_t launch_split_reduce(const SplitReduceProblem& p, const DeviceInfo& dev,
                                 cudaStream_t stream) {
   if (p.G <= 0) return cudaSuccess;
+  // The cluster form when a chunk's rows are whole 16-byte units, the CTAs
+  // of a row fit one portable cluster and their staging fits one CTA: as
+  // many CTAs per row (up to 8) as leave each at most kScMaxCpc chunks.
+  {
+    const int n_chunks = (p.B + kSrChunk - 1) / kSrChunk;
+    int cpc = std::max(1, (n_chunks + kScMaxCs - 1) / kScMaxCs);
+    const int cs = (n_chunks + cpc - 1) / cpc;
+    const size_t smem = split_cluster_smem(p.C, cpc, n_chunks);
+    const int64_t rows = static_cast<int64_t>(p.G) * p.R;
+    if (p.C % 8 == 0 && reinterpret_cast<uintptr_t>(p.partial_out) % 16 == 0 && cpc <= kScMaxCpc &&
+        cs <= kScMaxCs && smem + 1024 <= static_cast<size_t>(dev.max_smem_optin) &&
+        rows * cs <= 0x7FFFFFFFLL) {
+      ScArgs s;
+      s.pm = p.partial_max;
+      s.ps = p.partial_sum;
+      s.po = reinterpret_cast<const __half*>(p.partial_out);
+      s.out = p.out;
+      s.status = dev.status_word;
+      s.timeout_ns = kWaitTimeoutNs;
+      s.R = p.R;
+      s.B = p.B;
+      s.C = p.C;
+      s.cs = cs;
+      s.cpc = cpc;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(rows * cs));
+      cfg.blockDim = dim3(kScThreads);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[2];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      attr[1].id = cudaLaunchAttributeClusterDimension;
+      attr[1].val.clusterDim.x = static_cast<unsigned>(cs);
+      attr[1].val.clusterDim.y = 1;
+      attr[1].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 2;
+      plan_add("split_cluster_kernel");
+      return cudaLaunchKernelEx(&cfg, split_cluster_kernel, s);
+    }
+  }
   SrArgs a;
   a.pm = p.partial_max;
   a.ps = p.partial_sum;
