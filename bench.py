@@ -48,7 +48,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     "fused_step_kernel": {"bytes_per_launch": 1648640,
                           "sources": ["fused.cu", "select_row.cuh", "qsa_device.cuh"],
-                          "source_sha": "6c6f16051eb6c27c",
+                          "source_sha": "4173f3244eed8d83",
                           "workload": "long128k_nq256_h8_d128_kv131072"},
     "split_reduce_kernel": {"bytes_per_launch": 17387264,
                             "sources": ["split_reduce.cu", "qsa_device.cuh", "qsa_internal.h"],
