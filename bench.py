@@ -366,6 +366,16 @@ def run_ours(args):
                                     w.block, scores=sets.scores[v:v + nbat],
                                     ids=sets.ids[v:v + nbat])
 
+    def batched_shared(i):  # BB batches against one context's kb (a prefill's query batches)
+        j, r = divmod(i, n_launch)
+        nbat = min(BB, K - r * BB)
+        v = (j * K + r * BB) % sets.n
+        if v + nbat > sets.n:
+            v = 0
+        tbs.qsa_select_step_batched(sets.q32[v:v + nbat], sets.kb[v], w.n_kv, w.k, w.block,
+                                    q16=sets.q16[v:v + nbat], scores=sets.scores[v:v + nbat],
+                                    ids=sets.ids[v:v + nbat])
+
     def score_only(i):
         v = i % sets.n
         tbs.qsa_block_scores(sets.q16[v], sets.kb[v], w.n_kv, w.block, out=sets.scores[v])
@@ -389,7 +399,8 @@ def run_ours(args):
     replays = {name: rotating_replay(torch, stream, fn, cnt, n_sets) for name, fn, cnt, n_sets in
                (("step", step, K, sets.n), ("score", score_only, K, sets.n),
                 ("select", select_only, K, sets.n), ("convert", convert_only, K, sets.n),
-                ("batched", batched, n_launch, -(-sets.n // K) * n_launch))}
+                ("batched", batched, n_launch, -(-sets.n // K) * n_launch),
+                ("batched_shared", batched_shared, n_launch, -(-sets.n // K) * n_launch))}
     torch.cuda.synchronize()
 
     uuid = None
@@ -406,6 +417,11 @@ def run_ours(args):
     kern_ms = {name: statistics.median(time_region(torch, stream, replays[name], 5, 0.3))
                for name in ("score", "select", "convert")}
     batched_ms = time_region(torch, stream, replays["batched"], 5, 0.5, barrier if dist else None)
+    shared_ms = time_region(torch, stream, replays["batched_shared"], 5, 0.5, barrier if dist else None)
+    with torch.cuda.stream(stream):
+        batched_shared(0)
+    torch.cuda.synchronize()
+    shared_plan = tbs.qsa_arm().split("last call on this thread: ", 1)[-1]
 
     ms_step = statistics.median(step_ms) / K
     value = aggregate_rate(world, units_per_step(w) * K, statistics.median(step_ms))
@@ -463,6 +479,16 @@ def run_ours(args):
         "roofline_frac": (K * max(t_flop, t_byte)) / t_b,
         "api": "qsa_select_step_batched (per-batch kb, CUDA graph of K/B launches)",
     }
+    t_s = statistics.median(shared_ms) / 1e3
+    shared_res = {
+        "batches_per_call": BB, "calls": n_launch,
+        "value": world * units_per_step(w) * K / t_s, "unit": UNIT,
+        "ms_per_batch": t_s / K * 1e3,
+        "roofline_frac": (K * max(t_flop, t_byte)) / t_s,
+        "plan": shared_plan,
+        "api": "qsa_select_step_batched with one kb shared by the batches (a prefill's query "
+               "batches against one context), q16 buffer given; CUDA graph of K/B calls",
+    }
 
     # end-to-end through the host-buffer entry point
     e2e = run_e2e(torch, tbs, w, device, stream, K, W, barrier if dist else None, with_q16)
@@ -481,6 +507,7 @@ def run_ours(args):
         "roofline": roof,
         "separate_kernels": kernels,
         "batched": batched_res,
+        "batched_shared_kb": shared_res,
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,

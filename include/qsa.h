@@ -143,7 +143,7 @@ qsa_status qsa_select(const float* scores, int32_t nq, int32_t nb, int32_t k, in
  * then qsa_select, with the same arguments and rules as those two (and
  * bit-identical results). Both outputs are written: scores [nq, nb] and ids
  * [nq, k]. Up to a few waves of work this is one fused launch; a larger
- * problem (more than eight fused CTAs per SM, e.g. 4096 queries of 16 heads)
+ * problem (more than four fused CTAs per SM, e.g. 2048 queries of 8 heads)
  * runs the score, tail and select kernels in turn instead, chained by
  * programmatic dependent launch. The results are the same bits either way.
  */
@@ -184,8 +184,12 @@ int32_t qsa_select_step_launches(int32_t nq, int32_t H, int32_t D, int64_t n_kv,
  * qsa_select_step_batched / qsa_score_select_batched - n_batches independent
  * query batches in one launch (the selection phase's batch loop over query
  * batches, made one launch). Batch b is exactly qsa_select_step /
- * qsa_score_select on batch b's slices (bit-identical results), and always
- * one fused launch whatever the size:
+ * qsa_score_select on batch b's slices (bit-identical results). With
+ * per-batch keys (kb_batch_stride != 0) the call is one fused launch whatever
+ * the size; batches that share one kb (kb_batch_stride == 0) are one step
+ * over n_batches * nq queries and take the single-step plan (one fused
+ * launch, or for a large step given a q16 buffer the chain of separate
+ * kernels, as qsa_select_step / qsa_score_select):
  *   q32 / q     f32 / f16 [n_batches, nq, H, D]; q16 (optional) likewise.
  *   kb          f16: one [nb, D] shared by every batch when kb_batch_stride
  *               is 0 (the block keys of one context, shared by its query

@@ -479,8 +479,9 @@ def _batched_out(dev, n_batches, nq, nb, k, scores, ids):
 
 def qsa_select_step_batched(q32, kb, n_kv: int, k: int, block: int = 64, q16=None, scores=None,
                             ids=None):
-    """The step for q32 [n_batches, nq, H, D] in one launch; kb shared
-    ([nb, D]) or per batch ([n_batches, nb, D]). Returns (q16, scores, ids)."""
+    """The step for q32 [n_batches, nq, H, D]; kb shared ([nb, D]: one step
+    over every batch's queries) or per batch ([n_batches, nb, D]: one launch).
+    Returns (q16, scores, ids)."""
     torch = _torch()
     _need(q32, torch.float32, 4, "q32")
     B, nq, H, D = q32.shape

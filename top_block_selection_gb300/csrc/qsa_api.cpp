@@ -99,7 +99,7 @@ qsa_status run_scores(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t
 // which tiles 128 key blocks per MMA against many queries, does less work per
 // score. Both write identical scores and ids.
 bool use_separate(int32_t nq, int32_t H, const DeviceInfo& dev) {
-  return qsa::fused_blocks(nq, H, dev) > 8LL * dev.sm_count;
+  return qsa::fused_blocks(nq, H, dev) > 4LL * dev.sm_count;
 }
 
 qsa_status run_separate(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H, int32_t D,
@@ -274,6 +274,9 @@ qsa_status qsa_score_select_batched(const uint16_t* q, const uint16_t* kb, int64
   if (nq == 0 || n_batches == 0) return QSA_OK;
   if (static_cast<int64_t>(n_batches) * nq * H > 0x7FFFFFFFLL) return QSA_ERR_UNSUPPORTED_GEOMETRY;
   if (g.nb > 0 && (!q || !kb)) return QSA_ERR_INVALID_ARG;
+  // Batches sharing one kb: one step over n_batches * nq queries.
+  if (kb_batch_stride == 0)
+    return qsa_score_select(q, kb, n_batches * nq, H, D, n_kv, block, k, scores, ids, stream);
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
   qsa::FusedProblem p{nullptr, q,       nullptr,  kb, scores, ids, nq, H, D, g.nb, g.n_full,
@@ -295,6 +298,11 @@ qsa_status qsa_select_step_batched(const float* q32, uint16_t* q16, const uint16
   if (static_cast<int64_t>(n_batches) * nq * H > 0x7FFFFFFFLL) return QSA_ERR_UNSUPPORTED_GEOMETRY;
   if (!q32) return QSA_ERR_INVALID_ARG;
   if (!aligned(q32, 16) || !aligned(q16, 16)) return QSA_ERR_MISALIGNED;
+  // Batches sharing one kb are one step over n_batches * nq queries (the
+  // buffers are laid out as such): it takes the single-step plan, the chain
+  // of separate kernels when it is large and q16 is given.
+  if (kb_batch_stride == 0)
+    return qsa_select_step(q32, q16, kb, n_batches * nq, H, D, n_kv, block, k, scores, ids, stream);
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
   qsa::FusedProblem p{q32, nullptr, q16, kb, scores, ids, nq, H, D, g.nb, g.n_full,
