@@ -50,10 +50,10 @@ NCU_TRAFFIC = {
                           "sources": ["fused.cu", "select_row.cuh", "qsa_device.cuh"],
                           "source_sha": "4173f3244eed8d83",
                           "workload": "long128k_nq256_h8_d128_kv131072"},
-    "split_reduce_kernel": {"bytes_per_launch": 17387264,
-                            "sources": ["split_reduce.cu", "qsa_device.cuh", "qsa_internal.h"],
-                            "source_sha": "a09571c947151937",
-                            "workload": "split_g4_r8_c128_b2048"},
+    "split_cluster_kernel": {"bytes_per_launch": 17340544,
+                             "sources": ["split_reduce.cu", "qsa_device.cuh", "qsa_internal.h"],
+                             "source_sha": "be685f81be541f5b",
+                             "workload": "split_g4_r8_c128_b2048"},
 }
 
 
@@ -687,6 +687,8 @@ def run_split(torch, tbs, device, stream, peaks, peak_src, K, barrier):
     torch.cuda.synchronize()
     ms = time_region(torch, stream, replay, 5, 0.5, barrier)
     t = statistics.median(ms) / K / 1e3
+    plan = tbs.qsa_arm().split("last call on this thread: ", 1)[-1]
+    kname = plan.split(": ", 1)[-1].split(" ")[0]
     algo = 8.0 * w.G * w.R * w.B + 2.0 * w.G * w.R * w.B * w.C + 4.0 * w.G * w.R * w.C
     world = int(os.environ.get("WORLD_SIZE", "1"))
     return {
@@ -695,8 +697,8 @@ def run_split(torch, tbs, device, stream, peaks, peak_src, K, barrier):
         "us_per_call": t * 1e6, "launches_per_call": 1,
         "roofline": {"bound": "hbm", "achieved": algo / t / 1e9, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": algo / t / 1e9 / peaks["hbm_gbs"],
-                     "traffic": traffic_for("split_reduce_kernel", w), "algorithmic_bytes": algo,
-                     "peak_source": peak_src},
+                     "traffic": traffic_for(kname, w), "algorithmic_bytes": algo,
+                     "peak_source": peak_src, "kernel": kname, "plan": plan},
         "l2": f"rotating {n} input sets ({n * per_set / 2**20:.0f} MiB > 2x L2)",
         "api": "qsa_split_reduce (CUDA graph of K calls)",
     }

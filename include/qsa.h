@@ -278,7 +278,11 @@ qsa_status qsa_select_step_host_packed(const void* in_host, int32_t nq, int32_t 
  *                             qsa_device_status) returns early and may leave
  *                             them nonzero: zero-fill the workspace again
  *                             before its next use. Calls that may run at the
- *                             same time need separate workspaces.
+ *                             same time need separate workspaces. Shapes the
+ *                             one-cluster-per-row form takes (C % 8 == 0,
+ *                             partial_out 16-byte aligned, B <= 4096, a CTA's
+ *                             chunks fitting in its shared memory) leave the
+ *                             workspace untouched.
  * Arithmetic (fixed, so results are reproducible bit for bit on any GB300):
  * the blocks are reduced in chunks of 128 (the scales of a chunk staged on
  * chip), each chunk in runs of 32 blocks; in a run, sum and out accumulate

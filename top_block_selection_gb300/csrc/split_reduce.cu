@@ -390,12 +390,13 @@ __global__ void __launch_bounds__(kSrThreads) split_reduce_kernel(const SrArgs a
 // partial outputs (whole rows of C channels, one contiguous copy per chunk)
 // into shared memory and finds the maximum of its blocks' partial_max; each
 // CTA stores its maximum into every CTA's shared memory (distributed shared
-// memory), so after one cluster barrier every CTA has the row's maximum. It
+// memory), so once they have arrived every CTA has the row's maximum. It
 // then forms its chunks' partials in the fixed order (runs of 32 blocks
 // accumulated block by block, a chunk's runs added in order) and stores them
-// into CTA rank 0's shared memory; after a second cluster barrier rank 0
-// adds them in chunk order and divides. Every exchange is a store into the
-// reader's shared memory, so no CTA waits on a remote load. The arithmetic is the row-split kernel's,
+// into CTA rank 0's shared memory; once they have all arrived rank 0 adds
+// them in chunk order and divides. Every exchange is a remote store counted
+// on the reader's mbarrier (st.async), so no CTA waits on a remote load or on
+// a cluster-wide release. The arithmetic is the row-split kernel's,
 // operation for operation: the same bits, with no workspace, no arrival
 // counter and no global round trip. Only a few bytes per chunk cross between
 // CTAs (distributed shared memory moves bulk data slowly).
@@ -418,22 +419,23 @@ __device__ __forceinline__ uint32_t sc_cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void sc_cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
 // Stores v at the same shared-memory offset as `local` in CTA `rank` of the
-// cluster (a plain weak store; the next cluster barrier makes it visible).
-__device__ __forceinline__ void sc_st_peer(float* local, uint32_t rank, float v) {
-  uint32_t addr;
+// cluster (another CTA than the caller's), its 4 bytes counted on that CTA's
+// mbarrier at the offset of `bar`.
+__device__ __forceinline__ void sc_st_peer(float* local, uint32_t rank, float v, uint64_t* bar) {
+  uint32_t addr, baddr;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(baddr) : "r"(smem_u32(bar)), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(addr),
+               "r"(__float_as_uint(v)), "r"(baddr)
+               : "memory");
 }
 
 __global__ void __launch_bounds__(kScThreads)
     split_cluster_kernel(const ScArgs a) {
   extern __shared__ __align__(128) uint8_t sc_stage[];  // [cpc][128][C] fp16, then floats
   __shared__ __align__(8) uint64_t bar_chunk[kScMaxCpc];
+  __shared__ __align__(8) uint64_t bar_max, bar_gather;
   __shared__ float s_red[kScThreads / 32];
   __shared__ float s_lmax[kScMaxCs];  // every CTA's maximum, pushed by its owner
   __shared__ int s_ok;
@@ -457,7 +459,15 @@ __global__ void __launch_bounds__(kScThreads)
   pdl_launch_dependents();
   if (tid == 0) {
     for (int i = 0; i < kScMaxCpc; ++i) mbar_init(&bar_chunk[i], 1);
+    mbar_init(&bar_max, 1);
+    mbar_init(&bar_gather, 1);
     fence_mbarrier_init();
+    // Registered before the cluster's start barrier lets any peer store:
+    // the other CTAs' maxima here, and (rank 0) the other CTAs' chunk
+    // partials and sums. A CTA's own values go in with plain stores.
+    mbar_arrive_expect_tx(&bar_max, static_cast<uint32_t>(cs - 1) * 4u);
+    if (q == 0)
+      mbar_arrive_expect_tx(&bar_gather, static_cast<uint32_t>(n_chunks - (j1 - j0)) * (C + 1) * 4u);
     s_ok = 1;
     // this CTA's inputs on their way to L2 while the previous kernel
     // finishes (hints: they change no value a later load observes)
@@ -469,6 +479,10 @@ __global__ void __launch_bounds__(kScThreads)
     }
   }
   __syncthreads();
+  // Cluster start barrier: every CTA has started and initialised its
+  // barriers; arrived before the dependency wait, waited before the first
+  // remote store.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   pdl_wait();
   if (tid == 0) {
     for (int j = j0; j < j1; ++j) {
@@ -498,12 +512,20 @@ __global__ void __launch_bounds__(kScThreads)
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   if (lane == 0) s_red[warp] = m;
   __syncthreads();
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   if (tid < cs) {
     float mm = s_red[0];
     for (int w = 1; w < kScThreads / 32; ++w) mm = fmaxf(mm, s_red[w]);
-    sc_st_peer(&s_lmax[q], static_cast<uint32_t>(tid), mm);  // to CTA tid of the cluster
+    if (tid == q)
+      s_lmax[q] = mm;
+    else
+      sc_st_peer(&s_lmax[q], static_cast<uint32_t>(tid), mm, &bar_max);  // to CTA tid
   }
-  sc_cluster_sync();  // every CTA's maximum has reached every CTA
+  if (tid == 0 && !mbar_wait_bounded(&bar_max, 0, a.timeout_ns)) {
+    s_ok = 0;
+    atomicOr(a.status, kErrSplitLoadTimeout);
+  }
+  __syncthreads();  // every CTA's maximum has arrived here
   float M = s_lmax[0];
   for (int p = 1; p < cs; ++p) M = fmaxf(M, s_lmax[p]);
 #pragma unroll
@@ -572,10 +594,19 @@ __global__ void __launch_bounds__(kScThreads)
     for (int u = 0; u < nr; ++u)
       part = __fadd_rn(part, c < C ? run_out[(static_cast<size_t>(jl) * kSrRuns + u) * C + c]
                                    : run_sum[jl * kSrRuns + u]);
-    sc_st_peer(gather + static_cast<size_t>(j0 + jl) * (C + 1) + c, 0u, part);  // to rank 0
+    float* dst = gather + static_cast<size_t>(j0 + jl) * (C + 1) + c;
+    if (q == 0)
+      *dst = part;
+    else
+      sc_st_peer(dst, 0u, part, &bar_gather);  // to rank 0
   }
-  sc_cluster_sync();  // every chunk partial has reached rank 0
-  if (q == 0) {
+  if (q != 0) return;  // its stores are on their way; rank 0 waits for them
+  if (tid == 0 && !mbar_wait_bounded(&bar_gather, 0, a.timeout_ns)) {
+    s_ok = 0;
+    atomicOr(a.status, kErrSplitLoadTimeout);
+  }
+  __syncthreads();  // every chunk partial has arrived here
+  if (s_ok) {
     // chunk partials in chunk order, then the division
     for (int c = tid; c < C; c += kScThreads) {
       float tot = 0.0f, tot_s = 0.0f;
