@@ -590,8 +590,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(kLean ? 72 : 96)
       uint32_t key[8];
       if (a.dsmem) load_keys_regs<kWork, 8>(rk, a.nb, key, hist, tid);
       else load_keys_regs_global<kWork, 8>(row, a.nb, key, hist, tid);
-      if (!select_row_window<kWork, 8>(key, a.nb, a.k, out, hist, excl, cand, sel, sel_bin, sel_sh,
-                                     tid, 1)) {
+      if (!select_row_thr<kWork, 8>(key, a.nb, a.k, out, cand, sel_sh, tid, 1) &&
+          !select_row_window<kWork, 8>(key, a.nb, a.k, out, hist, excl, cand, sel, sel_bin, sel_sh,
+                                        tid, 1)) {
         build_first_digit_hist<kWork, 8>(key, a.nb, hist, tid, 1);
         select_row_regs<kWork, 8>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1);
       }
@@ -599,8 +600,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __maxnreg__(kLean ? 72 : 96)
       uint32_t key[16];
       if (a.dsmem) load_keys_regs<kWork, 16>(rk, a.nb, key, hist, tid);
       else load_keys_regs_global<kWork, 16>(row, a.nb, key, hist, tid);
-      if (!select_row_window<kWork, 16>(key, a.nb, a.k, out, hist, excl, cand, sel, sel_bin, sel_sh,
-                                      tid, 1)) {
+      if (!select_row_thr<kWork, 16>(key, a.nb, a.k, out, cand, sel_sh, tid, 1) &&
+          !select_row_window<kWork, 16>(key, a.nb, a.k, out, hist, excl, cand, sel, sel_bin, sel_sh,
+                                        tid, 1)) {
         build_first_digit_hist<kWork, 16>(key, a.nb, hist, tid, 1);
         select_row_regs<kWork, 16>(key, a.nb, a.k, out, hist, cand, sel, sel_sh, tid, 1);
       }

@@ -145,8 +145,9 @@ const char* qsa_arm(void) {
   thread_local char buf[1024];
   int n = snprintf(buf, sizeof buf,
                    "sm_103a: TMA + tcgen05.mma kind::f16 (M128, fp32 in TMEM) scorer with fused "
-                   "ReLU/head-sum epilogue; fp32 pinned-order tail (+1e9); radix top-k select "
-                   "(block-index tie-break); cvt.rn fp32->fp16 stage | last call on this thread: ");
+                   "ReLU/head-sum epilogue; fp32 pinned-order tail (+1e9); exact top-k select "
+                   "(threshold + rank for k <= 128, radix select otherwise; "
+                   "block-index tie-break); cvt.rn fp32->fp16 stage | last call on this thread: ");
   if (!t_plan_any) {
     snprintf(buf + n, sizeof buf - n, "none");
   } else if (t_plan_n == 0) {

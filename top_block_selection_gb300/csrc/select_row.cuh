@@ -6,9 +6,11 @@
 // tie-break): descending score; equal scores -> smaller block index first;
 // -0.0 == +0.0; ids past nb are -1.
 //
-// Scores are compared as order-preserving uint32 keys (score_key). The search
-// is a radix select on the keys, most significant digit first. Register-held
-// rows try a first digit measured down from the row's largest key
+// Scores are compared as order-preserving uint32 keys (score_key). For k <=
+// 128, register-held rows first try a threshold select (select_row_thr: a
+// lower bound of the k-th key from per-thread maxima, then an exact rank of
+// the few keys above it). Otherwise the search is a radix select on the keys,
+// most significant digit first. Register-held rows try a first digit measured down from the row's largest key
 // (select_row_window), which nearly always settles the search in one pass;
 // otherwise, and for rows in shared memory:
 //   * the first digit is fixed, the top 11 key bits (sign, exponent, two
@@ -500,6 +502,82 @@ __device__ bool select_row_window(const uint32_t (&key)[R], int nb, int k,
     out[r] = static_cast<int32_t>(~static_cast<uint32_t>(sel[e]));
   });
   for (int j = kk + gtid; j < k; j += T) out[j] = -1;
+  return true;
+}
+
+// ------------------------------------------- threshold select (registers)
+// For k <= kSelThrKMax and k < nb: a lower bound T of the k-th largest key
+// from per-thread maxima, then an exact rank of the few keys >= T.
+//   * each thread's R keys form a segment; warp w takes t_w, the q-th
+//     largest of its 32 segment maxima (q = ceil(k / warps)), by q rounds of
+//     a warp max with the round's maxima removed (equal maxima leave together,
+//     which can only lower t_w). At least q keys of warp w are >= t_w, so at
+//     least k keys of the row are >= T = min_w t_w: every winner is >= T.
+//   * the keys >= T (about 1.5-2 k on score rows) are gathered by a warp scan
+//     and one shared counter per warp, and each is ranked among them by
+//     (key, index) (split_rank); ranks below k are the output slots.
+// Two group barriers in all. Returns false, after a barrier and having
+// written nothing but cand and sh, when more than kSelBinMax keys are >= T
+// (ties or flat rows), or when k >= nb or k > kSelThrKMax; the caller then
+// runs the window select (hist must still be zero for it).
+// Measured against the window select on the same rows (one 256-thread CTA
+// per row, three per SM): 3,856 vs 4,297 cycles per 2048-key row, 2,646 vs
+// 3,800 per 513-key row. Gathering into per-warp slots without the shared
+// counter, or ranking with warp sums, or sorting the candidates with one
+// warp's bitonic network were each slower (4,365 / 5,557 cycles): shuffles
+// and warp reductions are the scarce resource when several CTAs share an SM.
+constexpr int kSelThrKMax = 128;
+
+template <int T, int R>
+__device__ bool select_row_thr(const uint32_t (&key)[R], int nb, int k, int32_t* __restrict__ out,
+                               uint64_t* cand, SelectShared& sh, int gtid, int bar_id) {
+  constexpr int kWarps = T / 32;
+  if (k >= nb || k > kSelThrKMax) return false;
+  const int lane = gtid & 31, warp = gtid >> 5;
+  const int q = (k + kWarps - 1) / kWarps;
+  uint32_t m = 0;  // keys past nb are 0, below every score's key
+#pragma unroll
+  for (int j = 0; j < R; ++j) m = max(m, key[j]);
+  uint32_t v = m, t = 0;
+  for (int i = 0; i < q; ++i) {
+    t = __reduce_max_sync(0xFFFFFFFFu, v);
+    if (v == t) v = 0;
+  }
+  if (lane == 0) sh.wsum[warp] = t;
+  if (gtid == 0) sh.n_cand = 0;
+  group_sync<T>(bar_id);
+  uint32_t thr = 0xFFFFFFFFu;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) thr = min(thr, sh.wsum[w]);
+  uint32_t c = 0;
+#pragma unroll
+  for (int j = 0; j < R; ++j) c += (j * T + gtid < nb && key[j] >= thr) ? 1u : 0u;
+  uint32_t incl = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += x;
+  }
+  uint32_t base = 0;
+  if (lane == 31) base = atomicAdd(&sh.n_cand, incl);
+  base = __shfl_sync(0xFFFFFFFFu, base, 31);
+  uint32_t o = base + incl - c;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    if (j * T + gtid < nb && key[j] >= thr) {
+      if (o < static_cast<uint32_t>(kSelBinMax)) cand[o] = win_key(key[j], j * T + gtid);
+      ++o;
+    }
+  }
+  group_sync<T>(bar_id);
+  const uint32_t n_c = sh.n_cand;
+  if (n_c > static_cast<uint32_t>(kSelBinMax)) {
+    group_sync<T>(bar_id);  // every thread has read n_cand before sh is reused
+    return false;
+  }
+  split_rank<T>(cand, static_cast<int>(n_c), gtid, [&](int e, uint32_t r) {
+    if (r < static_cast<uint32_t>(k)) out[r] = static_cast<int32_t>(~static_cast<uint32_t>(cand[e]));
+  });
   return true;
 }
 
