@@ -212,7 +212,7 @@ def test_arm_reports_the_plan_that_ran(tbs):
     torch.cuda.synchronize()
     arm = tbs.qsa_arm()
     assert ("3 launches: convert_vec8_kernel -> score_tc_persistent_kernel -> "
-            "select_window_kernel") in arm, arm
+            "select_warp_kernel") in arm, arm
     assert tbs.qsa_select_step_launches(nq, H, 128, nb * 64, 64, 64, with_q16=True) == 3
 
 
@@ -336,6 +336,20 @@ def test_select_exact(tbs, kind, nb, k):
     s = qi.random_scores(nq, nb, seed=nb * 31 + k, kind=kind)
     ids = tbs.qsa_select(dev(s), k)
     torch.cuda.synchronize()
+    assert np.array_equal(ids.cpu().numpy(), orc.select_topk(s, k))
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties", "signed0", "const"])
+@pytest.mark.parametrize("nb,k", [(1, 1), (5, 8), (100, 64), (129, 128), (2049, 64), (4096, 128)])
+def test_select_exact_many_rows(tbs, kind, nb, k):
+    """Launches of many rows take the one-warp-per-row select: exact against
+    the oracle on score rows, ties, signed zeros and constant rows (the last
+    two take its bisection path)."""
+    nq = 1100
+    s = qi.random_scores(nq, nb, seed=nb * 17 + k, kind=kind)
+    ids = tbs.qsa_select(dev(s), k)
+    torch.cuda.synchronize()
+    assert "select_warp_kernel" in tbs.qsa_arm()
     assert np.array_equal(ids.cpu().numpy(), orc.select_topk(s, k))
 
 

@@ -23,7 +23,7 @@ LIBPATH = os.path.join(LIBDIR, "libqsa.so")
 
 SOURCES = ["qsa_runtime.cu", "score_tc.cu", "select.cu", "convert.cu", "fused.cu", "split_reduce.cu",
            "split_reduce_static.cu", "qsa_api.cpp"]
-HEADERS = ["qsa_device.cuh", "qsa_internal.h", "select_row.cuh"]
+HEADERS = ["qsa_device.cuh", "qsa_internal.h", "select_row.cuh", "select_warp.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -18,8 +18,8 @@
 // The [nq*H, n_full] pre-activation matrix never leaves TMEM and registers.
 //
 // Tail block (Strata pull request 856, "What": the shared tail kernel and the
-// +1e9 dead-tail rule): one thread per (query, head) sums the fp32 products
-// over i in order; one thread per query then sums max(acc_h, 0) over h in
+// +1e9 dead-tail rule): the rows of q staged in shared memory, one thread per
+// (query, head) sums the fp32 products over i in order; one thread per query then sums max(acc_h, 0) over h in
 // order and adds 1e9f. Every step is a round-to-nearest-even fp32 operation
 // (no contraction, no reassociation), so the result is reproducible bit for
 // bit.
@@ -363,23 +363,41 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (warp == kPProducerWarp) tmem_dealloc(tmem_base, 2u * a.tmem_cols);
 }
 
+// Tail block: one CTA per kTailThreads (query, head) rows (whole queries),
+// the rows staged in shared memory by coalesced 16-byte copies (row stride
+// 2 D + 16 bytes, so each thread's 16-byte reads of its own row are free of
+// bank conflicts); thread r then sums row r's products in index order, and
+// one thread per query sums its heads' max(acc, 0) in head order and adds
+// 1e9f.
 __global__ void __launch_bounds__(kTailThreads)
     tail_kernel(const __half* __restrict__ q, const __half* __restrict__ kb_tail,
                 float* __restrict__ scores, int32_t nq, int32_t H, int32_t D, int64_t nb) {
+  extern __shared__ __align__(16) uint8_t tail_rows[];
   __shared__ float acc_s[kTailThreads];
   pdl_launch_dependents();
   pdl_wait();
   const int q_per_block = kTailThreads / H;
-  const int ql = threadIdx.x / H;
-  const int h = threadIdx.x - ql * H;
-  const int64_t qi = static_cast<int64_t>(blockIdx.x) * q_per_block + ql;
-  const bool active = ql < q_per_block && qi < nq;
+  const int64_t q0 = static_cast<int64_t>(blockIdx.x) * q_per_block;
+  const int64_t row0 = q0 * H;
+  const int rows = static_cast<int>(min(static_cast<int64_t>(q_per_block), static_cast<int64_t>(nq) - q0)) * H;
+  const int stride = 2 * D + 16;
+  const int units = D / 8;  // 16-byte units per row
+  // 16-byte asynchronous copies, all in flight at once (q and its rows are
+  // 16-byte aligned: D % 16 == 0).
+  for (int u = threadIdx.x; u < rows * units; u += kTailThreads) {
+    const int r = u / units, c = u - r * units;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(tail_rows + r * stride + c * 16)),
+                 "l"(reinterpret_cast<uint64_t>(q + (row0 + r) * D + c * 8))
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
   float acc = 0.0f;
-  if (active) {
-    const __half* qr = q + (qi * H + h) * D;
+  if (static_cast<int>(threadIdx.x) < rows) {
+    const uint8_t* rp = tail_rows + threadIdx.x * stride;
     for (int i = 0; i < D; i += 8) {
-      const uint4 qv = *reinterpret_cast<const uint4*>(qr + i);
-      const uint4 kv = *reinterpret_cast<const uint4*>(kb_tail + i);
+      const uint4 qv = *reinterpret_cast<const uint4*>(rp + i * 2);
+      const uint4 kv = __ldg(reinterpret_cast<const uint4*>(kb_tail + i));
       const __half* qh = reinterpret_cast<const __half*>(&qv);
       const __half* kh = reinterpret_cast<const __half*>(&kv);
 #pragma unroll
@@ -389,11 +407,16 @@ __global__ void __launch_bounds__(kTailThreads)
   }
   acc_s[threadIdx.x] = acc;
   __syncthreads();
-  if (active && h == 0) {
+  const int ql = threadIdx.x;
+  if (ql * H < rows) {
     float t = 0.0f;
     for (int hh = 0; hh < H; ++hh) t = __fadd_rn(t, fmaxf(acc_s[ql * H + hh], 0.0f));
-    scores[qi * nb + (nb - 1)] = __fadd_rn(t, 1.0e9f);
+    scores[(q0 + ql) * nb + (nb - 1)] = __fadd_rn(t, 1.0e9f);
   }
+}
+
+inline size_t tail_smem_bytes(int32_t D) {
+  return static_cast<size_t>(kTailThreads) * (2 * static_cast<size_t>(D) + 16);
 }
 
 // ------------------------------------------------------------------ host
@@ -478,6 +501,12 @@ int choose_bn(int64_t m_tiles, int64_t cols, int sm_count) {
 }  // namespace
 
 cudaError_t init_score_kernels(const DeviceInfo& dev) {
+  {
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&tail_kernel),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(tail_smem_bytes(256)));
+    if (e != cudaSuccess) return e;
+  }
   for (int H : {1, 2, 4, 8, 16, 32}) {
     for (const void* fn : {score_kernel_for(H), persistent_kernel_for(H)}) {
       cudaFuncAttributes fa;
@@ -538,8 +567,8 @@ cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStre
         const int q_per_block = kTailThreads / p.H;
         const int64_t grid = (p.nq + q_per_block - 1) / q_per_block;
         plan_add("tail_kernel");
-        return launch_pdl(tail_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTailThreads), 0,
-                          stream, reinterpret_cast<const __half*>(p.q),
+        return launch_pdl(tail_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTailThreads),
+                          tail_smem_bytes(p.D), stream, reinterpret_cast<const __half*>(p.q),
                           reinterpret_cast<const __half*>(p.kb) + (p.nb - 1) * p.D, p.scores,
                           p.nq, p.H, p.D, p.nb);
       }
@@ -566,7 +595,8 @@ cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStre
     const int q_per_block = kTailThreads / p.H;
     const int64_t grid = (p.nq + q_per_block - 1) / q_per_block;
     plan_add("tail_kernel");
-    return launch_pdl(tail_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTailThreads), 0, stream,
+    return launch_pdl(tail_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTailThreads),
+                      tail_smem_bytes(p.D), stream,
                       reinterpret_cast<const __half*>(p.q),
                       reinterpret_cast<const __half*>(p.kb) + (p.nb - 1) * p.D, p.scores, p.nq,
                       p.H, p.D, p.nb);

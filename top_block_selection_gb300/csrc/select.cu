@@ -10,8 +10,11 @@
 // are staged in shared memory, the first 11-bit radix digit finds the
 // boundary bin, the boundary bin's keys are compacted and refined, and the
 // winners are rank-sorted.
+#include <algorithm>
+
 #include "qsa_internal.h"
 #include "select_row.cuh"
+#include "select_warp.cuh"
 
 namespace qsa {
 
@@ -102,7 +105,56 @@ __global__ void __launch_bounds__(kWinThreads, 3)
   }
 }
 
+constexpr int kWsWarps = 8;
+constexpr int kWsMaxNb = 4096;
+constexpr int kWsMinRows = 1024;  // fewer rows: one CTA per row has the lower latency
+
+// Shared bytes of the warp select kernel: per warp, kWarpSelCap candidates
+// and the row's keys (nb rounded up to 4 words).
+inline size_t select_warp_bytes(int32_t nb) {
+  return static_cast<size_t>(kWsWarps) *
+         (kWarpSelCap * sizeof(uint64_t) + ((static_cast<size_t>(nb) + 3) & ~static_cast<size_t>(3)) * 4);
+}
+
+__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+
+// Many rows: one warp per row, rows grid-strided over the launch's warps.
+// The row is staged into the warp's slice of shared memory by 4-byte
+// asynchronous copies (all in flight at once; rows need not be 16-byte
+// aligned) and selected there (select_row_warp_f32).
+__global__ void __launch_bounds__(kWsWarps * 32)
+    select_warp_kernel(const float* __restrict__ scores, int32_t nq, int32_t nb, int32_t k,
+                       int32_t* __restrict__ ids) {
+  extern __shared__ __align__(16) uint8_t sm_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row_words = (nb + 3) & ~3;
+  uint64_t* cand = reinterpret_cast<uint64_t*>(sm_raw) + warp * kWarpSelCap;
+  float* buf = reinterpret_cast<float*>(sm_raw + kWsWarps * kWarpSelCap * sizeof(uint64_t)) +
+               warp * row_words;
+  pdl_launch_dependents();
+  pdl_wait();  // the scores may come from the previous kernel on the stream
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWsWarps + warp; row < nq;
+       row += static_cast<int64_t>(gridDim.x) * kWsWarps) {
+    const float* s = scores + row * nb;
+    for (int i = lane; i < nb; i += 32) cp_async_4(buf + i, s + i);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+    select_row_warp_f32(buf, nb, k, ids + row * k, cand, lane);
+    __syncwarp();  // the slice is rewritten by the next row
+  }
+}
+
 cudaError_t init_select_kernels(const DeviceInfo& dev) {
+  {
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&select_warp_kernel),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(select_warp_bytes(kWsMaxNb)));
+    if (e != cudaSuccess) return e;
+  }
   for (const void* fn : {reinterpret_cast<const void*>(&select_window_kernel<8>),
                          reinterpret_cast<const void*>(&select_window_kernel<12>),
                          reinterpret_cast<const void*>(&select_window_kernel<16>)}) {
@@ -121,6 +173,18 @@ cudaError_t init_select_kernels(const DeviceInfo& dev) {
 cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k, int32_t* ids,
                           const DeviceInfo& dev, cudaStream_t stream) {
   if (nq <= 0) return cudaSuccess;
+  if (nq >= kWsMinRows && nb >= 1 && nb <= kWsMaxNb && k <= kWarpSelKMax) {
+    const size_t smem = select_warp_bytes(nb);
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_warp_kernel,
+                                                                  kWsWarps * 32, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t want = (static_cast<int64_t>(nq) + kWsWarps - 1) / kWsWarps;
+    const int64_t grid = std::min(want, static_cast<int64_t>(std::max(per_sm, 1)) * dev.sm_count);
+    plan_add("select_warp_kernel");
+    return launch_pdl(select_warp_kernel, dim3(static_cast<unsigned>(grid)), dim3(kWsWarps * 32),
+                      smem, stream, scores, nq, nb, k, ids);
+  }
   if (nb >= 1 && nb <= 16 * kWinThreads && k <= 1024) {
     const size_t smem = select_window_bytes(k);
     const dim3 grid(static_cast<unsigned>(nq)), block(kWinThreads);
