@@ -86,9 +86,9 @@ qsa_status check_select(const float* scores, int32_t nq, int64_t nb, int32_t k,
 
 qsa_status run_scores(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H, int32_t D,
                       const Geometry& g, float* scores, const DeviceInfo& dev,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool skip_tail = false) {
   if (nq == 0 || g.nb == 0) return QSA_OK;
-  qsa::ScoreProblem p{q, kb, scores, nq, H, D, g.nb, g.n_full, g.has_tail};
+  qsa::ScoreProblem p{q, kb, scores, nq, H, D, g.nb, g.n_full, g.has_tail, skip_tail};
   return from_cuda(qsa::launch_scores(p, dev, stream));
 }
 
@@ -102,12 +102,18 @@ bool use_separate(int32_t nq, int32_t H, const DeviceInfo& dev) {
   return qsa::fused_blocks(nq, H, dev) > 4LL * dev.sm_count;
 }
 
+// With many rows the select kernel scores the tail column itself (one launch
+// fewer; the same pinned fp32 order, so the same bits).
 qsa_status run_separate(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H, int32_t D,
                         const Geometry& g, int32_t k, float* scores, int32_t* ids,
                         const DeviceInfo& dev, cudaStream_t stream) {
-  qsa_status st = run_scores(q, kb, nq, H, D, g, scores, dev, stream);
+  const int32_t nb = static_cast<int32_t>(g.nb);
+  const bool tail_in_select = g.has_tail && qsa::select_scores_tail(nq, nb, k);
+  qsa_status st = run_scores(q, kb, nq, H, D, g, scores, dev, stream, tail_in_select);
   if (st != QSA_OK) return st;
-  return from_cuda(qsa::launch_select(scores, nq, static_cast<int32_t>(g.nb), k, ids, dev, stream));
+  if (!tail_in_select) return from_cuda(qsa::launch_select(scores, nq, nb, k, ids, dev, stream));
+  const qsa::TailInfo t{q, kb + (g.nb - 1) * D, H, D};
+  return from_cuda(qsa::launch_select(scores, nq, nb, k, ids, dev, stream, &t));
 }
 
 }  // namespace
@@ -250,9 +256,10 @@ int32_t qsa_select_step_launches(int32_t nq, int32_t H, int32_t D, int64_t n_kv,
   if (device_or_error(&dev, false) != QSA_OK) return -1;
   if (!with_q16 || !use_separate(nq, H, *dev)) return 1;
   // convert (nq * H * D is a multiple of 8: one vector launch), the score
-  // kernel when there are full blocks, the tail kernel when there is a tail,
-  // and the select.
-  return 1 + (n_kv / block > 0 ? 1 : 0) + (n_kv % block != 0 ? 1 : 0) + 1;
+  // kernel when there are full blocks, the tail kernel when there is a tail
+  // that the select does not score itself, and the select.
+  const bool tail_kernel = n_kv % block != 0 && !qsa::select_scores_tail(nq, static_cast<int32_t>(nb), k);
+  return 1 + (n_kv / block > 0 ? 1 : 0) + (tail_kernel ? 1 : 0) + 1;
 }
 
 // Shared by the two batched entry points: batch count and kb stride rules.

@@ -72,6 +72,7 @@ struct ScoreProblem {
   int32_t nq, H, D;
   int64_t nb, n_full;
   bool has_tail;
+  bool skip_tail;  // the tail column is left to the select (select_scores_tail)
 };
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStream_t stream);
@@ -98,8 +99,19 @@ cudaError_t init_fused_kernels(const DeviceInfo& dev);
 int64_t fused_blocks(int32_t nq, int32_t H, const DeviceInfo& dev);
 cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStream_t stream);
 
+// The tail block of a chained step, scored by the select kernel itself (fp16
+// queries [nq, H, D] and the tail's key row); see select_scores_tail.
+struct TailInfo {
+  const uint16_t* q16;
+  const uint16_t* kb_tail;
+  int32_t H, D;
+};
+// True when launch_select with a TailInfo scores the tail column (column nb-1)
+// itself before selecting: many rows, k <= 128, nb <= 4096.
+bool select_scores_tail(int32_t nq, int32_t nb, int32_t k);
 cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k, int32_t* ids,
-                          const DeviceInfo& dev, cudaStream_t stream);
+                          const DeviceInfo& dev, cudaStream_t stream,
+                          const TailInfo* tail = nullptr);
 
 // Launches the bounded-wait self-test (see qsa_selftest_bounded_wait).
 cudaError_t launch_selftest_wait(const DeviceInfo& dev, uint64_t timeout_ns, cudaStream_t stream);

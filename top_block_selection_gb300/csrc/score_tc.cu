@@ -563,7 +563,7 @@ cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStre
         default: break;
       }
       if (e != cudaSuccess) return e;
-      if (p.nq > 0 && p.has_tail) {
+      if (p.nq > 0 && p.has_tail && !p.skip_tail) {
         const int q_per_block = kTailThreads / p.H;
         const int64_t grid = (p.nq + q_per_block - 1) / q_per_block;
         plan_add("tail_kernel");
@@ -591,7 +591,7 @@ cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStre
     }
     if (e != cudaSuccess) return e;
   }
-  if (p.nq > 0 && p.has_tail) {
+  if (p.nq > 0 && p.has_tail && !p.skip_tail) {
     const int q_per_block = kTailThreads / p.H;
     const int64_t grid = (p.nq + q_per_block - 1) / q_per_block;
     plan_add("tail_kernel");

@@ -12,6 +12,8 @@
 // winners are rank-sorted.
 #include <algorithm>
 
+#include <cuda_fp16.h>
+
 #include "qsa_internal.h"
 #include "select_row.cuh"
 #include "select_warp.cuh"
@@ -126,9 +128,18 @@ __device__ __forceinline__ void cp_async_4(void* smem_dst, const void* src) {
 // The row is staged into the warp's slice of shared memory by 4-byte
 // asynchronous copies (all in flight at once; rows need not be 16-byte
 // aligned) and selected there (select_row_warp_f32).
+// kTail: the row's last column is the tail block (Strata pull request 856,
+// "What": the shared tail kernel and the +1e9 dead-tail rule), scored here
+// while the copies are in flight: lane h < H sums head h's fp32 products in
+// index order, lane 0 sums max(acc_h, 0) in head order and adds 1e9f (the
+// pinned order of the tail kernel, every step round-to-nearest-even); the
+// score goes to the scores row and into the staged row before the select.
+template <bool kTail>
 __global__ void __launch_bounds__(kWsWarps * 32)
-    select_warp_kernel(const float* __restrict__ scores, int32_t nq, int32_t nb, int32_t k,
-                       int32_t* __restrict__ ids) {
+    select_warp_kernel(const float* scores_in, float* scores_tail,
+                       int32_t nq, int32_t nb, int32_t k, int32_t* __restrict__ ids,
+                       const __half* __restrict__ q16, const __half* __restrict__ kb_tail,
+                       int32_t H, int32_t D) {
   extern __shared__ __align__(16) uint8_t sm_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row_words = (nb + 3) & ~3;
@@ -136,24 +147,53 @@ __global__ void __launch_bounds__(kWsWarps * 32)
   float* buf = reinterpret_cast<float*>(sm_raw + kWsWarps * kWarpSelCap * sizeof(uint64_t)) +
                warp * row_words;
   pdl_launch_dependents();
-  pdl_wait();  // the scores may come from the previous kernel on the stream
+  pdl_wait();  // the scores (and q16) may come from earlier kernels on the stream
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWsWarps + warp; row < nq;
        row += static_cast<int64_t>(gridDim.x) * kWsWarps) {
-    const float* s = scores + row * nb;
-    for (int i = lane; i < nb; i += 32) cp_async_4(buf + i, s + i);
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    const float* s = scores_in + row * nb;
+    const int n_copy = kTail ? nb - 1 : nb;
+    for (int i = lane; i < n_copy; i += 32) cp_async_4(buf + i, s + i);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    float tail = 0.0f;
+    if constexpr (kTail) {
+      float acc = 0.0f;
+      if (lane < H) {
+        const __half* qr = q16 + (row * H + lane) * D;
+        for (int i = 0; i < D; i += 8) {
+          const uint4 qv = __ldg(reinterpret_cast<const uint4*>(qr + i));
+          const uint4 kv = __ldg(reinterpret_cast<const uint4*>(kb_tail + i));
+          const __half* qh = reinterpret_cast<const __half*>(&qv);
+          const __half* kh = reinterpret_cast<const __half*>(&kv);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            acc = __fadd_rn(acc, __fmul_rn(__half2float(qh[j]), __half2float(kh[j])));
+        }
+      }
+      float t = 0.0f;
+      for (int h = 0; h < H; ++h) t = __fadd_rn(t, fmaxf(__shfl_sync(0xFFFFFFFFu, acc, h), 0.0f));
+      tail = __fadd_rn(t, 1.0e9f);
+      if (lane == 0) scores_tail[row * nb + (nb - 1)] = tail;
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (kTail && lane == 0) buf[nb - 1] = tail;
     __syncwarp();
     select_row_warp_f32(buf, nb, k, ids + row * k, cand, lane);
     __syncwarp();  // the slice is rewritten by the next row
   }
 }
 
+bool select_scores_tail(int32_t nq, int32_t nb, int32_t k) {
+  return nq >= kWsMinRows && nb >= 2 && nb <= kWsMaxNb && k <= kWarpSelKMax;
+}
+
 cudaError_t init_select_kernels(const DeviceInfo& dev) {
   {
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&select_warp_kernel),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(select_warp_bytes(kWsMaxNb)));
-    if (e != cudaSuccess) return e;
+    for (const void* fn : {reinterpret_cast<const void*>(&select_warp_kernel<false>),
+                           reinterpret_cast<const void*>(&select_warp_kernel<true>)}) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(select_warp_bytes(kWsMaxNb)));
+      if (e != cudaSuccess) return e;
+    }
   }
   for (const void* fn : {reinterpret_cast<const void*>(&select_window_kernel<8>),
                          reinterpret_cast<const void*>(&select_window_kernel<12>),
@@ -171,19 +211,25 @@ cudaError_t init_select_kernels(const DeviceInfo& dev) {
 }
 
 cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k, int32_t* ids,
-                          const DeviceInfo& dev, cudaStream_t stream) {
+                          const DeviceInfo& dev, cudaStream_t stream, const TailInfo* tail) {
   if (nq <= 0) return cudaSuccess;
+  if (tail != nullptr && !select_scores_tail(nq, nb, k)) return cudaErrorInvalidValue;
   if (nq >= kWsMinRows && nb >= 1 && nb <= kWsMaxNb && k <= kWarpSelKMax) {
     const size_t smem = select_warp_bytes(nb);
+    auto fn = tail != nullptr ? select_warp_kernel<true> : select_warp_kernel<false>;
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_warp_kernel,
-                                                                  kWsWarps * 32, smem);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kWsWarps * 32, smem);
     if (e != cudaSuccess) return e;
     const int64_t want = (static_cast<int64_t>(nq) + kWsWarps - 1) / kWsWarps;
     const int64_t grid = std::min(want, static_cast<int64_t>(std::max(per_sm, 1)) * dev.sm_count);
-    plan_add("select_warp_kernel");
-    return launch_pdl(select_warp_kernel, dim3(static_cast<unsigned>(grid)), dim3(kWsWarps * 32),
-                      smem, stream, scores, nq, nb, k, ids);
+    plan_add(tail != nullptr ? "select_warp_kernel (tail block scored in)" : "select_warp_kernel");
+    // scores is written (the tail column) only in the tail form
+    float* scores_w = const_cast<float*>(scores);
+    return launch_pdl(fn, dim3(static_cast<unsigned>(grid)), dim3(kWsWarps * 32), smem, stream,
+                      scores, scores_w, nq, nb, k, ids,
+                      tail ? reinterpret_cast<const __half*>(tail->q16) : nullptr,
+                      tail ? reinterpret_cast<const __half*>(tail->kb_tail) : nullptr,
+                      tail ? tail->H : 0, tail ? tail->D : 0);
   }
   if (nb >= 1 && nb <= 16 * kWinThreads && k <= 1024) {
     const size_t smem = select_window_bytes(k);
