@@ -156,17 +156,25 @@ __global__ void __launch_bounds__(kWsWarps * 32)
     asm volatile("cp.async.commit_group;" ::: "memory");
     float tail = 0.0f;
     if constexpr (kTail) {
+      // acc = fl(acc + q_i k_i) for i in order. A product of two fp16 values
+      // is exact in fp32, so one fused multiply-add per step rounds exactly as
+      // the separate multiply and add do.
       float acc = 0.0f;
       if (lane < H) {
-        const __half* qr = q16 + (row * H + lane) * D;
-        for (int i = 0; i < D; i += 8) {
+        const __half2* qr = reinterpret_cast<const __half2*>(q16 + (row * H + lane) * D);
+        const __half2* kr = reinterpret_cast<const __half2*>(kb_tail);
+#pragma unroll 8
+        for (int i = 0; i < D / 2; i += 4) {  // eight 16-byte loads of q in flight
           const uint4 qv = __ldg(reinterpret_cast<const uint4*>(qr + i));
-          const uint4 kv = __ldg(reinterpret_cast<const uint4*>(kb_tail + i));
-          const __half* qh = reinterpret_cast<const __half*>(&qv);
-          const __half* kh = reinterpret_cast<const __half*>(&kv);
+          const uint4 kv = __ldg(reinterpret_cast<const uint4*>(kr + i));
+          const __half2* qh = reinterpret_cast<const __half2*>(&qv);
+          const __half2* kh = reinterpret_cast<const __half2*>(&kv);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            acc = __fadd_rn(acc, __fmul_rn(__half2float(qh[j]), __half2float(kh[j])));
+          for (int j = 0; j < 4; ++j) {
+            const float2 qf = __half22float2(qh[j]), kf = __half22float2(kh[j]);
+            acc = __fmaf_rn(qf.x, kf.x, acc);
+            acc = __fmaf_rn(qf.y, kf.y, acc);
+          }
         }
       }
       float t = 0.0f;
