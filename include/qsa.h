@@ -66,7 +66,7 @@ const char* qsa_status_str(qsa_status status);
 /* NUL-terminated description of the arm (the kernels this library runs),
  * followed by the plan the last launching call on this thread ran: the
  * number of launches and each kernel by name, in order (for example one
- * select_step_kernel launch, or a chain of convert, score, tail and select
+ * fused_step_kernel launch, or a chain of convert, score and select
  * kernels), or "none" before any such call. So a fallback cannot pass for
  * the fast path (after Strata pull request 228, part 1, which prints the arm
  * that ran). The text lives in thread-local storage: valid until the next
@@ -144,8 +144,11 @@ qsa_status qsa_select(const float* scores, int32_t nq, int32_t nb, int32_t k, in
  * bit-identical results). Both outputs are written: scores [nq, nb] and ids
  * [nq, k]. Up to a few waves of work this is one fused launch; a larger
  * problem (more than four fused CTAs per SM, e.g. 2048 queries of 8 heads)
- * runs the score, tail and select kernels in turn instead, chained by
- * programmatic dependent launch. The results are the same bits either way.
+ * runs the score and select kernels in turn instead, chained by
+ * programmatic dependent launch; the tail block is scored by the select
+ * kernel when it selects one row per warp (at least 1024 rows, k <= 128,
+ * nb <= 4096), else by a tail kernel between the two. The results are the
+ * same bits either way.
  */
 qsa_status qsa_score_select(const uint16_t* q, const uint16_t* kb, int32_t nq, int32_t H,
                             int32_t D, int64_t n_kv, int32_t block, int32_t k, float* scores,
