@@ -234,6 +234,30 @@ def test_large_scorer_ragged(tbs, nq, H, n_kv):
         assert s[:, -1].view(np.uint32).tolist() == tail.view(np.uint32).tolist()
 
 
+@pytest.mark.parametrize("nq,H,n_kv,k", [(1300, 8, 700 * 64 + 5, 32), (1100, 32, 300 * 64 + 1, 64)])
+def test_chain_with_tail_in_select(tbs, nq, H, n_kv, k):
+    """Steps too large for one fused launch, with a tail block and at least
+    1024 rows: the chain's one-warp-per-row select scores the tail itself
+    (H lanes, one per head). Bit for bit with the fused kernel, the tail
+    bitwise against the oracle, the ids the oracle's top-k of the same
+    scores."""
+    q, kb = qi.random_case(nq, H, 128, -(-n_kv // 64), seed=nq * 7 + H, scale=0.25)
+    qd, kd = dev(q), dev(kb)
+    s_c, i_c = tbs.qsa_score_select(qd, kd, n_kv, k, 64)
+    torch.cuda.synchronize()
+    arm = tbs.qsa_arm()
+    assert "select_warp_kernel (tail block scored in)" in arm and "tail_kernel" not in arm, arm
+    s_f, i_f = tbs.qsa_score_select_batched(qd[None], kd, n_kv, k, 64)
+    torch.cuda.synchronize()
+    assert torch.equal(s_c.view(torch.int32), s_f[0].view(torch.int32))
+    assert torch.equal(i_c, i_f[0])
+    s = s_c.cpu().numpy()
+    s_ref, S, B, tail = orc.reference_scores(q, kb, n_kv, 64)
+    assert orc.bound_report(s, s_ref, B)["ok"]
+    assert s[:, -1].view(np.uint32).tolist() == tail.view(np.uint32).tolist()
+    assert np.array_equal(i_c.cpu().numpy(), orc.select_topk(s, k))
+
+
 def test_select_step_without_q16_output(tbs):
     w = qi.WORKLOADS[0]
     q32, _ = qi.make_f32_inputs(w)
