@@ -363,7 +363,7 @@ def run_ours(args):
         if v + nbat > sets.n:
             v = 0
         tbs.qsa_select_step_batched(sets.q32[v:v + nbat], sets.kb[v:v + nbat], w.n_kv, w.k,
-                                    w.block, scores=sets.scores[v:v + nbat],
+                                    w.block, q16=sets.q16[v:v + nbat], scores=sets.scores[v:v + nbat],
                                     ids=sets.ids[v:v + nbat])
 
     def batched_shared(i):  # BB batches against one context's kb (a prefill's query batches)
@@ -418,6 +418,10 @@ def run_ours(args):
                for name in ("score", "select", "convert")}
     batched_ms = time_region(torch, stream, replays["batched"], 5, 0.5, barrier if dist else None)
     shared_ms = time_region(torch, stream, replays["batched_shared"], 5, 0.5, barrier if dist else None)
+    with torch.cuda.stream(stream):
+        batched(0)
+    torch.cuda.synchronize()
+    batched_plan = tbs.qsa_arm().split("last call on this thread: ", 1)[-1]
     with torch.cuda.stream(stream):
         batched_shared(0)
     torch.cuda.synchronize()
@@ -477,7 +481,9 @@ def run_ours(args):
         "value": world * units_per_step(w) * K / t_b, "unit": UNIT,
         "ms_per_batch": t_b / K * 1e3,
         "roofline_frac": (K * max(t_flop, t_byte)) / t_b,
-        "api": "qsa_select_step_batched (per-batch kb, CUDA graph of K/B launches)",
+        "plan": batched_plan,
+        "api": "qsa_select_step_batched with a kb per batch, q16 buffer given; CUDA graph of K/B "
+               "calls",
     }
     t_s = statistics.median(shared_ms) / 1e3
     shared_res = {

@@ -300,6 +300,54 @@ def test_batched_step_equals_single_steps(tbs, w, shared_kb):
     assert np.array_equal(ib[1].cpu().numpy(), orc.select_topk(s1, w.k))
 
 
+def test_batched_per_batch_kb_chain(tbs):
+    """Eight batches of the 128K workload, each with its own kb, and a q16
+    buffer: past a few waves of the fused kernel they run as the chain
+    (conversion, persistent scores over every batch's tiles, one select over
+    every batch's rows). Bit for bit with single-batch steps."""
+    w = qi.BY_NAME["long128k_nq256_h8_d128_kv131072"]
+    B = 8
+    q32 = np.stack([qi.make_f32_inputs(w, variant=v)[0] for v in range(B)])
+    kbs = np.stack([qi.make_inputs(w, variant=v)[1] for v in range(B)])
+    q16b, sb, ib = tbs.qsa_select_step_batched(dev(q32), dev(kbs), w.n_kv, w.k, w.block,
+                                               q16=torch.empty(q32.shape, dtype=torch.float16,
+                                                               device="cuda"))
+    torch.cuda.synchronize()
+    arm = tbs.qsa_arm()
+    assert "score_tc_persistent_kernel" in arm and "select_warp_kernel" in arm, arm
+    for b in (0, 5, 7):
+        q16s, ss, is_ = tbs.qsa_select_step(dev(q32[b]), dev(kbs[b]), w.n_kv, w.k, w.block,
+                                            q16=torch.empty(q32.shape[1:], dtype=torch.float16,
+                                                            device="cuda"))
+        torch.cuda.synchronize()
+        assert torch.equal(sb[b].view(torch.int32), ss.view(torch.int32)), b
+        assert torch.equal(ib[b], is_), b
+        assert torch.equal(q16b[b].view(torch.int16), q16s.view(torch.int16)), b
+
+
+@pytest.mark.parametrize("nq,H,n_kv,B", [(256, 16, 700 * 64 + 9, 8), (512, 8, 1000 * 64 + 1, 5)])
+def test_batched_per_batch_kb_chain_with_tail(tbs, nq, H, n_kv, B):
+    """The per-batch-kb chain with a tail block: each batch's tail is scored
+    by the select with that batch's key row. Bit for bit with the fused
+    kernel on each batch; tails bitwise against the oracle."""
+    nb = -(-n_kv // 64)
+    qs, kbs = zip(*[qi.random_case(nq, H, 128, nb, seed=31 * b + nq, scale=0.25) for b in range(B)])
+    q, kb = np.stack(qs), np.stack(kbs)
+    s_c, i_c = tbs.qsa_score_select_batched(dev(q), dev(kb), n_kv, 64, 64)
+    torch.cuda.synchronize()
+    arm = tbs.qsa_arm()
+    assert "select_warp_kernel (tail block scored in)" in arm, arm
+    for b in range(B):
+        s_f, i_f = tbs.qsa_score_select_batched(dev(q[b])[None], dev(kb[b]), n_kv, 64, 64)
+        torch.cuda.synchronize()
+        assert torch.equal(s_c[b].view(torch.int32), s_f[0].view(torch.int32)), b
+        assert torch.equal(i_c[b], i_f[0]), b
+    s_ref, S, B_, tail = orc.reference_scores(q[B - 1], kb[B - 1], n_kv, 64)
+    s = s_c[B - 1].cpu().numpy()
+    assert s[:, -1].view(np.uint32).tolist() == tail.view(np.uint32).tolist()
+    assert orc.bound_report(s, s_ref, B_)["ok"]
+
+
 @pytest.mark.parametrize("nq,nb,n_batches", [(256, 2048, 3), (64, 3000, 6)])
 def test_batched_lean_form(tbs, nq, nb, n_batches):
     """Launches of several waves take the lean form (one Kb stage, capped

@@ -116,6 +116,40 @@ qsa_status run_separate(const uint16_t* q, const uint16_t* kb, int32_t nq, int32
   return from_cuda(qsa::launch_select(scores, nq, nb, k, ids, dev, stream, &t));
 }
 
+// Batches with their own kb: past a few waves of the fused kernel the chain
+// (persistent scores over every batch's tiles, then one select over every
+// batch's rows, the tail block scored there) does the same work with less
+// per score, when the persistent kernel and the row select can take it.
+bool batched_chain_ok(int32_t n_batches, int32_t nq, int32_t H, int32_t D, const Geometry& g, int32_t k,
+                      int64_t kb_batch_stride, const DeviceInfo& dev) {
+  if (n_batches < 2 || g.nb == 0 || g.n_full == 0) return false;
+  const int64_t rows = static_cast<int64_t>(n_batches) * nq;
+  if (rows > 0x7FFFFFFFLL) return false;
+  if (static_cast<int64_t>(n_batches) * qsa::fused_blocks(nq, H, dev) <= 4LL * dev.sm_count) return false;
+  qsa::ScoreProblem sp{nullptr, nullptr, nullptr, nq, H, D, g.nb, g.n_full, g.has_tail, g.has_tail};
+  sp.n_batches = n_batches;
+  sp.kb_batch_stride = kb_batch_stride;
+  if (!qsa::scores_persistent(sp, dev)) return false;
+  return !g.has_tail || qsa::select_scores_tail(static_cast<int32_t>(rows), static_cast<int32_t>(g.nb), k);
+}
+
+qsa_status run_batched_chain(const uint16_t* q, const uint16_t* kb, int64_t kb_batch_stride,
+                             int32_t n_batches, int32_t nq, int32_t H, int32_t D, const Geometry& g,
+                             int32_t k, float* scores, int32_t* ids, const DeviceInfo& dev,
+                             cudaStream_t stream) {
+  qsa::ScoreProblem sp{q, kb, scores, nq, H, D, g.nb, g.n_full, g.has_tail, g.has_tail};
+  sp.n_batches = n_batches;
+  sp.kb_batch_stride = kb_batch_stride;
+  qsa_status st = from_cuda(qsa::launch_scores(sp, dev, stream));
+  if (st != QSA_OK) return st;
+  const int32_t rows = n_batches * nq, nb = static_cast<int32_t>(g.nb);
+  if (!g.has_tail) return from_cuda(qsa::launch_select(scores, rows, nb, k, ids, dev, stream));
+  qsa::TailInfo t{q, kb + (g.nb - 1) * D, H, D};
+  t.kb_batch_stride = kb_batch_stride;
+  t.nq_per_batch = nq;
+  return from_cuda(qsa::launch_select(scores, rows, nb, k, ids, dev, stream, &t));
+}
+
 }  // namespace
 
 namespace qsa {
@@ -287,6 +321,9 @@ qsa_status qsa_score_select_batched(const uint16_t* q, const uint16_t* kb, int64
     return qsa_score_select(q, kb, n_batches * nq, H, D, n_kv, block, k, scores, ids, stream);
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  if (batched_chain_ok(n_batches, nq, H, D, g, k, kb_batch_stride, *dev))
+    return run_batched_chain(q, kb, kb_batch_stride, n_batches, nq, H, D, g, k, scores, ids, *dev,
+                             as_cuda(stream));
   qsa::FusedProblem p{nullptr, q,       nullptr,  kb, scores, ids, nq, H, D, g.nb, g.n_full,
                       g.has_tail, k, n_batches, kb_batch_stride};
   return from_cuda(qsa::launch_fused(p, *dev, as_cuda(stream)));
@@ -313,6 +350,12 @@ qsa_status qsa_select_step_batched(const float* q32, uint16_t* q16, const uint16
     return qsa_select_step(q32, q16, kb, n_batches * nq, H, D, n_kv, block, k, scores, ids, stream);
   const DeviceInfo* dev = nullptr;
   if ((st = device_or_error(&dev)) != QSA_OK) return st;
+  if (q16 && batched_chain_ok(n_batches, nq, H, D, g, k, kb_batch_stride, *dev)) {
+    cudaStream_t s = as_cuda(stream);
+    const int64_t n = static_cast<int64_t>(n_batches) * nq * H * D;
+    if ((st = from_cuda(qsa::launch_convert(q32, q16, n, *dev, s))) != QSA_OK) return st;
+    return run_batched_chain(q16, kb, kb_batch_stride, n_batches, nq, H, D, g, k, scores, ids, *dev, s);
+  }
   qsa::FusedProblem p{q32, nullptr, q16, kb, scores, ids, nq, H, D, g.nb, g.n_full,
                       g.has_tail, k, n_batches, kb_batch_stride};
   return from_cuda(qsa::launch_fused(p, *dev, as_cuda(stream)));

@@ -73,8 +73,18 @@ struct ScoreProblem {
   int64_t nb, n_full;
   bool has_tail;
   bool skip_tail;  // the tail column is left to the select (select_scores_tail)
+  // n_batches > 1: that many batches of nq queries, q, scores contiguous per
+  // batch; kb per batch at kb_batch_stride elements (0: one kb shared). Only
+  // the persistent kernel takes batches (scores_persistent), with skip_tail
+  // or no tail.
+  int32_t n_batches = 1;
+  int64_t kb_batch_stride = 0;
 };
-// Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
+// True when launch_scores runs the persistent score kernel for p (many
+// full-width tiles; the only form that takes batches).
+bool scores_persistent(const ScoreProblem& p, const DeviceInfo& dev);
+// Returns cudaErrorInvalidValue if a tensor map cannot be encoded, or for
+// batches the persistent kernel cannot take.
 cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStream_t stream);
 
 // The fused step: optional fp32->fp16 conversion of q, block scores (full
@@ -103,8 +113,10 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
 // queries [nq, H, D] and the tail's key row); see select_scores_tail.
 struct TailInfo {
   const uint16_t* q16;
-  const uint16_t* kb_tail;
+  const uint16_t* kb_tail;  // the tail's key row (of batch 0)
   int32_t H, D;
+  int64_t kb_batch_stride = 0;  // elements between batches' kb; 0: one kb
+  int32_t nq_per_batch = 1;     // rows of one batch (used when kb_batch_stride != 0)
 };
 // True when launch_select with a TailInfo scores the tail column (column nb-1)
 // itself before selecting: many rows, k <= 128, nb <= 4096.

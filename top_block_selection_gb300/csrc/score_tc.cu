@@ -46,6 +46,7 @@ struct ScoreArgs {
   uint32_t tmem_cols;  // power of two >= bn
   uint32_t* status;
   uint64_t timeout_ns;
+  int32_t kb_z;        // persistent kernel: 1 when each batch has its own kb (3rd map coordinate)
 };
 
 template <int H>
@@ -175,7 +176,10 @@ __device__ __forceinline__ void mbar_arrive_local(uint64_t* bar) {
 }
 
 struct PersistArgs {
-  int64_t m_tiles, tiles;  // tiles = m_tiles * n_tiles
+  int64_t m_tiles, tiles;  // tiles = n_batches * n_tiles_b * m_tiles
+  int64_t n_tiles_b;       // column tiles of one batch (batches never share a column tile)
+  int64_t rows_per_batch;  // nq * H: q rows of one batch
+  int64_t scores_per_batch;  // nq * nb
 };
 
 template <int H>
@@ -235,7 +239,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       uint32_t qf_phase = 0, q_loads_issued_phase = 0;
       const uint32_t q_bytes = static_cast<uint32_t>(a.n_chunks * a.bn * kRowBytes);
       for (int64_t i = 0; i < count && !failed; ++i) {
+        // tile t: column tile g (batch g / n_tiles_b), block tile m
         const int64_t t = t0 + i, n = t / pa.m_tiles, m = t - n * pa.m_tiles;
+        const int64_t bt = n / pa.n_tiles_b, nb_ = n - bt * pa.n_tiles_b;
         if (n != cur_n) {
           if (cur_n >= 0) {  // every MMA on the previous query tile has completed
             if (!mbar_wait_bounded(&q_free, qf_phase, a.timeout_ns)) { failed = 1; break; }
@@ -244,8 +250,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (cur_n >= 0) q_loads_issued_phase ^= 1u;  // phase of the load issued now
           mbar_arrive_expect_tx(&q_full, q_bytes);
           for (int c = 0; c < a.n_chunks; ++c)
-            tma_load_2d(sQ + c * a.bn * kRowBytes, &tm_q, c * kKAtom, static_cast<int32_t>(n * a.bn),
-                        &q_full);
+            tma_load_2d(sQ + c * a.bn * kRowBytes, &tm_q, c * kKAtom,
+                        static_cast<int32_t>(bt * pa.rows_per_batch + nb_ * a.bn), &q_full);
           cur_n = n;
         }
         const int s = static_cast<int>(i % kPStages);
@@ -256,8 +262,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(a_bytes));
         for (int c = 0; c < a.n_chunks; ++c)
-          tma_load_2d(sA + s * a_bytes + c * kTileM * kRowBytes, &tm_kb, c * kKAtom,
-                      static_cast<int32_t>(m * kTileM), &full[s]);
+          tma_load_3d(sA + s * a_bytes + c * kTileM * kRowBytes, &tm_kb, c * kKAtom,
+                      static_cast<int32_t>(m * kTileM), a.kb_z ? static_cast<int32_t>(bt) : 0, &full[s]);
         issued = i + 1;
       }
       if (failed) {
@@ -326,10 +332,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       tc_fence_after_sync();
       const int64_t t = t0 + i, n = t / pa.m_tiles, m = t - n * pa.m_tiles;
+      const int64_t bt = n / pa.n_tiles_b, nb_ = n - bt * pa.n_tiles_b;
       const int b = static_cast<int>(m) * kTileM + lane_base + lane;
       const bool b_ok = b < a.n_full;
-      float* out = a.scores + b;
-      const int q0 = static_cast<int>(n) * a.q_per_tile;
+      float* out = a.scores + bt * pa.scores_per_batch + b;
+      const int q0 = static_cast<int>(nb_) * a.q_per_tile;
       const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc) * a.tmem_cols +
                              (static_cast<uint32_t>(lane_base) << 16);
       for (int cb = c_begin; cb < c_begin + half_cols; cb += 128) {
@@ -488,6 +495,21 @@ bool encode_2d_f16(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D fp16 map [z][rows][cols] with a z stride in elements (a multiple of 8).
+bool encode_3d_f16(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint64_t zs,
+                   uint64_t z_stride, uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {cols, rows, zs};
+  const cuuint64_t strides[2] = {cols * 2, z_stride * 2};
+  const cuuint32_t box[3] = {box_cols, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Columns per tile: the widest of 256/128/64/32 that still gives at least one
 // CTA per SM; narrower tiles spread small problems over more SMs.
 int choose_bn(int64_t m_tiles, int64_t cols, int sm_count) {
@@ -520,17 +542,47 @@ cudaError_t init_score_kernels(const DeviceInfo& dev) {
   return cudaSuccess;
 }
 
+namespace {
+// The persistent kernel's plan for p (batches included): full-width tiles
+// (256 columns), at least four per SM, and its shared memory within bounds.
+struct PersistPlan {
+  bool ok;
+  int bn;
+  int64_t m_tiles, n_tiles_b, tiles;
+};
+PersistPlan persistent_plan(const ScoreProblem& p, const DeviceInfo& dev) {
+  PersistPlan pp{false, 0, 0, 0, 0};
+  if (p.nq <= 0 || p.n_full <= 0) return pp;
+  const int64_t nbat = p.n_batches > 1 ? p.n_batches : 1;
+  const int64_t cols_b = static_cast<int64_t>(p.nq) * p.H;
+  pp.m_tiles = (p.n_full + kTileM - 1) / kTileM;
+  pp.bn = choose_bn(pp.m_tiles, nbat * cols_b, dev.sm_count);
+  pp.n_tiles_b = (cols_b + pp.bn - 1) / pp.bn;
+  pp.tiles = nbat * pp.n_tiles_b * pp.m_tiles;
+  const int n_chunks = (p.D + kKAtom - 1) / kKAtom;
+  const size_t psmem = static_cast<size_t>(n_chunks) * (pp.bn + kPStages * kTileM) * kRowBytes + 1024;
+  pp.ok = pp.bn == 256 && pp.tiles >= 4LL * dev.sm_count &&
+          psmem <= static_cast<size_t>(dev.max_smem_optin) - 1024;
+  return pp;
+}
+}  // namespace
+
+bool scores_persistent(const ScoreProblem& p, const DeviceInfo& dev) { return persistent_plan(p, dev).ok; }
+
 cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStream_t stream) {
+  const PersistPlan pp = persistent_plan(p, dev);
+  // Several batches (each with its own kb, or one shared) run only on the
+  // persistent kernel, with the tail left to the select.
+  if (p.n_batches > 1 && (!pp.ok || (p.has_tail && !p.skip_tail))) return cudaErrorInvalidValue;
   if (p.nq > 0 && p.n_full > 0) {
+    const int64_t nbat = p.n_batches > 1 ? p.n_batches : 1;
     const int64_t cols = static_cast<int64_t>(p.nq) * p.H;
     const int64_t m_tiles = (p.n_full + kTileM - 1) / kTileM;
-    const int bn = choose_bn(m_tiles, cols, dev.sm_count);
+    const int bn = pp.ok ? pp.bn : choose_bn(m_tiles, cols, dev.sm_count);
     const int64_t n_tiles = (cols + bn - 1) / bn;
     if (m_tiles > 0x7FFFFFFF || n_tiles > 65535) return cudaErrorInvalidValue;
     CUtensorMap tm_kb, tm_q;
-    if (!encode_2d_f16(&tm_kb, p.kb, p.D, p.n_full, kKAtom, kTileM) ||
-        !encode_2d_f16(&tm_q, p.q, p.D, cols, kKAtom, bn))
-      return cudaErrorInvalidValue;
+    if (!encode_2d_f16(&tm_q, p.q, p.D, nbat * cols, kKAtom, bn)) return cudaErrorInvalidValue;
     ScoreArgs a;
     a.scores = p.scores;
     a.nq = p.nq;
@@ -543,12 +595,16 @@ cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStre
     a.tmem_cols = tmem_cols_for(bn);
     a.status = dev.status_word;
     a.timeout_ns = kWaitTimeoutNs;
+    a.kb_z = p.kb_batch_stride != 0 ? 1 : 0;
     // Many full-width tiles: the persistent kernel (one CTA per SM, pipelined
     // loads, MMAs and epilogue); the same arithmetic per score.
     const size_t psmem = static_cast<size_t>(a.n_chunks) * (bn + kPStages * kTileM) * kRowBytes + 1024;
-    if (bn == 256 && m_tiles * n_tiles >= 4LL * dev.sm_count &&
-        psmem <= static_cast<size_t>(dev.max_smem_optin) - 1024) {
-      PersistArgs pa{m_tiles, m_tiles * n_tiles};
+    if (pp.ok) {
+      const uint64_t zs = p.kb_batch_stride != 0 ? static_cast<uint64_t>(nbat) : 1u;
+      const uint64_t zst = p.kb_batch_stride != 0 ? static_cast<uint64_t>(p.kb_batch_stride)
+                                                  : static_cast<uint64_t>(p.n_full) * p.D;
+      if (!encode_3d_f16(&tm_kb, p.kb, p.D, p.n_full, zs, zst, kKAtom, kTileM)) return cudaErrorInvalidValue;
+      PersistArgs pa{pp.m_tiles, pp.tiles, pp.n_tiles_b, cols, static_cast<int64_t>(p.nq) * p.nb};
       const dim3 pgrid(static_cast<unsigned>(std::min<int64_t>(dev.sm_count, pa.tiles)));
       const dim3 pblock(kPThreads);
       plan_add("score_tc_persistent_kernel");
@@ -574,6 +630,7 @@ cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStre
       }
       return cudaSuccess;
     }
+    if (!encode_2d_f16(&tm_kb, p.kb, p.D, p.n_full, kKAtom, kTileM)) return cudaErrorInvalidValue;
     const size_t smem = score_smem_bytes(bn, a.n_chunks, a.tmem_cols);
     if (smem > static_cast<size_t>(dev.max_smem_optin)) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(m_tiles), static_cast<unsigned>(n_tiles));

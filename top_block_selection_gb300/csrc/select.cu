@@ -11,6 +11,9 @@
 // boundary bin, the boundary bin's keys are compacted and refined, and the
 // winners are rank-sorted.
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include <cuda_fp16.h>
 
@@ -138,8 +141,8 @@ template <bool kTail>
 __global__ void __launch_bounds__(kWsWarps * 32)
     select_warp_kernel(const float* scores_in, float* scores_tail,
                        int32_t nq, int32_t nb, int32_t k, int32_t* __restrict__ ids,
-                       const __half* __restrict__ q16, const __half* __restrict__ kb_tail,
-                       int32_t H, int32_t D) {
+                       const __half* __restrict__ q16, const __half* __restrict__ kb_tail0,
+                       int32_t H, int32_t D, int64_t kb_batch_stride, int32_t nq_per_batch) {
   extern __shared__ __align__(16) uint8_t sm_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row_words = (nb + 3) & ~3;
@@ -160,6 +163,8 @@ __global__ void __launch_bounds__(kWsWarps * 32)
       // is exact in fp32, so one fused multiply-add per step rounds exactly as
       // the separate multiply and add do.
       float acc = 0.0f;
+      const __half* kb_tail =
+          kb_tail0 + (kb_batch_stride != 0 ? (row / nq_per_batch) * kb_batch_stride : 0);
       if (lane < H) {
         const __half2* qr = reinterpret_cast<const __half2*>(q16 + (row * H + lane) * D);
         const __half2* kr = reinterpret_cast<const __half2*>(kb_tail);
@@ -225,9 +230,24 @@ cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k
   if (nq >= kWsMinRows && nb >= 1 && nb <= kWsMaxNb && k <= kWarpSelKMax) {
     const size_t smem = select_warp_bytes(nb);
     auto fn = tail != nullptr ? select_warp_kernel<true> : select_warp_kernel<false>;
+    // CTAs per SM for this row length, asked of the runtime once per (device,
+    // form, shared bytes): the query is host work that eager callers would
+    // otherwise pay on every call.
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kWsWarps * 32, smem);
-    if (e != cudaSuccess) return e;
+    {
+      static std::mutex mu;
+      static std::map<std::tuple<int, bool, size_t>, int> cache;
+      const auto key = std::make_tuple(dev.id, tail != nullptr, smem);
+      std::lock_guard<std::mutex> lock(mu);
+      auto it = cache.find(key);
+      if (it != cache.end()) {
+        per_sm = it->second;
+      } else {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kWsWarps * 32, smem);
+        if (e != cudaSuccess) return e;
+        cache.emplace(key, per_sm);
+      }
+    }
     const int64_t want = (static_cast<int64_t>(nq) + kWsWarps - 1) / kWsWarps;
     const int64_t grid = std::min(want, static_cast<int64_t>(std::max(per_sm, 1)) * dev.sm_count);
     plan_add(tail != nullptr ? "select_warp_kernel (tail block scored in)" : "select_warp_kernel");
@@ -237,7 +257,8 @@ cudaError_t launch_select(const float* scores, int32_t nq, int32_t nb, int32_t k
                       scores, scores_w, nq, nb, k, ids,
                       tail ? reinterpret_cast<const __half*>(tail->q16) : nullptr,
                       tail ? reinterpret_cast<const __half*>(tail->kb_tail) : nullptr,
-                      tail ? tail->H : 0, tail ? tail->D : 0);
+                      tail ? tail->H : 0, tail ? tail->D : 0, tail ? tail->kb_batch_stride : 0,
+                      tail ? tail->nq_per_batch : 1);
   }
   if (nb >= 1 && nb <= 16 * kWinThreads && k <= 1024) {
     const size_t smem = select_window_bytes(k);
