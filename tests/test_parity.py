@@ -325,7 +325,8 @@ def test_batched_per_batch_kb_chain(tbs):
         assert torch.equal(q16b[b].view(torch.int16), q16s.view(torch.int16)), b
 
 
-@pytest.mark.parametrize("nq,H,n_kv,B", [(256, 16, 700 * 64 + 9, 8), (512, 8, 1000 * 64 + 1, 5)])
+@pytest.mark.parametrize("nq,H,n_kv,B", [(256, 16, 700 * 64 + 9, 8), (512, 8, 1000 * 64 + 1, 5),
+                                        (300, 8, 1500 * 64 + 3, 8)])
 def test_batched_per_batch_kb_chain_with_tail(tbs, nq, H, n_kv, B):
     """The per-batch-kb chain with a tail block: each batch's tail is scored
     by the select with that batch's key row. Bit for bit with the fused
