@@ -21,9 +21,10 @@ LIBDIR = os.path.join(HERE, "lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIBPATH = os.path.join(LIBDIR, "libqsa.so")
 
-SOURCES = ["qsa_runtime.cu", "score_tc.cu", "select.cu", "convert.cu", "fused.cu", "split_reduce.cu",
-           "split_reduce_static.cu", "qsa_api.cpp"]
-HEADERS = ["qsa_device.cuh", "qsa_internal.h", "select_row.cuh", "select_warp.cuh"]
+SOURCES = ["qsa_runtime.cu", "score_tc.cu", "select.cu", "convert.cu", "fused.cu", "fused_h1.cu",
+           "fused_h2.cu", "fused_h4.cu", "fused_h8.cu", "fused_h16.cu", "fused_h32.cu",
+           "split_reduce.cu", "split_reduce_static.cu", "qsa_api.cpp"]
+HEADERS = ["qsa_device.cuh", "qsa_internal.h", "select_row.cuh", "select_warp.cuh", "fused_kernel.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

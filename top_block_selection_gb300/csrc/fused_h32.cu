@@ -1,0 +1,7 @@
+// fused_h32.cu - the fused step kernel's instantiations for 32 heads (one
+// translation unit per head count, so that they compile in parallel).
+#include "fused_kernel.cuh"
+
+namespace qsa {
+const void* fused_kernel_h32(bool f32q, int form) { return fused_kernel_ptr<32>(f32q, form); }
+}  // namespace qsa
