@@ -1,6 +1,10 @@
 // fused.cu - host side of the fused step kernel (fused_kernel.cuh): the
 // choice of form and cluster size, shared-memory layout, tensor maps and the
 // launch. The kernels themselves are instantiated in fused_h{1,...,32}.cu.
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "fused_kernel.cuh"
 
 namespace qsa {
@@ -94,7 +98,26 @@ int64_t fused_blocks(int32_t nq, int32_t H, const DeviceInfo& dev) {
   return ((static_cast<int64_t>(nq) + qg - 1) / qg) * kCluster;
 }
 
-cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStream_t stream) {
+namespace {
+// Whether a cluster of the wide form fits the device with this launch's
+// shared memory (asked of the runtime once per kernel and size): if not, the
+// launch takes the 8-CTA form instead of failing.
+bool wide_fits(const void* fn, const cudaLaunchConfig_t& cfg, const DeviceInfo& dev) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, size_t>, bool> cache;
+  const auto key = std::make_tuple(dev.id, fn, cfg.dynamicSmemBytes);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  const bool ok = cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess && n >= 1;
+  cudaGetLastError();  // a refused query leaves no sticky error behind
+  cache.emplace(key, ok);
+  return ok;
+}
+
+cudaError_t launch_fused_impl(const FusedProblem& p, const DeviceInfo& dev, cudaStream_t stream,
+                              bool allow_wide) {
   if (p.nq <= 0) return cudaSuccess;
   const int bn = fused_bn(p.nq, p.H, dev);
   const int qg = bn / p.H;
@@ -103,8 +126,8 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
   // Wide form (16-CTA clusters) for one or two clusters with at least one
   // block tile per CTA: decode-shaped steps, where most SMs are idle and each
   // CTA's kb load and MMA chain halve.
-  const bool wide = static_cast<int64_t>(p.n_batches) * groups <= 2 && m_tiles >= kClusterWide &&
-                    bn % kClusterWide == 0;
+  const bool wide = allow_wide && static_cast<int64_t>(p.n_batches) * groups <= 2 &&
+                    m_tiles >= kClusterWide && bn % kClusterWide == 0;
   const int cluster = wide ? kClusterWide : kCluster;
   const int64_t blocks = static_cast<int64_t>(p.n_batches) * groups * cluster;
   if (blocks > 0x7FFFFFFFLL || groups > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
@@ -178,9 +201,6 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
   const bool f32q = p.q32 != nullptr;
   const void* fn = fused_kernel_for(p.H, f32q, wide ? kFormWide : lean ? kFormLean : kFormRegular);
   if (fn == nullptr) return cudaErrorInvalidValue;
-  plan_add(wide   ? "fused_step_kernel (16-CTA clusters)"
-           : lean ? "fused_step_kernel (8-CTA clusters, lean form)"
-                  : "fused_step_kernel (8-CTA clusters)");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kFThreads);
@@ -195,10 +215,20 @@ cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStrea
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  if (wide && !wide_fits(fn, cfg, dev)) return launch_fused_impl(p, dev, stream, false);
+  plan_add(wide   ? "fused_step_kernel (16-CTA clusters)"
+           : lean ? "fused_step_kernel (8-CTA clusters, lean form)"
+                  : "fused_step_kernel (8-CTA clusters)");
   void* args[] = {&tm_kb, &tm_q, &a};
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fused(const FusedProblem& p, const DeviceInfo& dev, cudaStream_t stream) {
+  return launch_fused_impl(p, dev, stream, true);
 }
 
 }  // namespace qsa
