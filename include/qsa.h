@@ -188,11 +188,18 @@ int32_t qsa_select_step_launches(int32_t nq, int32_t H, int32_t D, int64_t n_kv,
  * query batches in one launch (the selection phase's batch loop over query
  * batches, made one launch). Batch b is exactly qsa_select_step /
  * qsa_score_select on batch b's slices (bit-identical results). With
- * per-batch keys (kb_batch_stride != 0) the call is one fused launch whatever
- * the size; batches that share one kb (kb_batch_stride == 0) are one step
- * over n_batches * nq queries and take the single-step plan (one fused
- * launch, or for a large step given a q16 buffer the chain of separate
- * kernels, as qsa_select_step / qsa_score_select):
+ * per-batch keys (kb_batch_stride != 0) the call is one fused launch while
+ * that is at most about four CTAs per SM; past that (and, for
+ * qsa_select_step_batched, given a q16 buffer) it runs the chain: one
+ * conversion of every batch's queries, one persistent score launch over
+ * every batch's tiles and one select launch over every batch's rows (which
+ * scores each batch's tail block), when those kernels can take the sizes
+ * (at least four 128 x 256 tiles per SM; with a tail, at least 1024 rows in
+ * all, k <= 128, nb <= 4096), else the fused launch. Batches that share one
+ * kb (kb_batch_stride == 0) are one step over n_batches * nq queries and
+ * take the single-step plan (one fused launch, or for a large step given a
+ * q16 buffer the chain of separate kernels, as qsa_select_step /
+ * qsa_score_select):
  *   q32 / q     f32 / f16 [n_batches, nq, H, D]; q16 (optional) likewise.
  *   kb          f16: one [nb, D] shared by every batch when kb_batch_stride
  *               is 0 (the block keys of one context, shared by its query
