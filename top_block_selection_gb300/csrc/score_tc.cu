@@ -204,6 +204,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int64_t bx = blockIdx.x;
   const int64_t t0 = bx * per + (bx < extra ? bx : extra);
   const int64_t count = per + (blockIdx.x < extra ? 1 : 0);
+  const int32_t m_tiles32 = static_cast<int32_t>(pa.m_tiles);
+  const int32_t n_tiles_b32 = static_cast<int32_t>(pa.n_tiles_b);
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
@@ -240,8 +242,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const uint32_t q_bytes = static_cast<uint32_t>(a.n_chunks * a.bn * kRowBytes);
       for (int64_t i = 0; i < count && !failed; ++i) {
         // tile t: column tile g (batch g / n_tiles_b), block tile m
-        const int64_t t = t0 + i, n = t / pa.m_tiles, m = t - n * pa.m_tiles;
-        const int64_t bt = n / pa.n_tiles_b, nb_ = n - bt * pa.n_tiles_b;
+        // 32-bit index arithmetic: the host keeps tiles below 2^31
+        const int32_t t = static_cast<int32_t>(t0 + i), n = t / m_tiles32, m = t - n * m_tiles32;
+        const int32_t bt = n / n_tiles_b32, nb_ = n - bt * n_tiles_b32;
         if (n != cur_n) {
           if (cur_n >= 0) {  // every MMA on the previous query tile has completed
             if (!mbar_wait_bounded(&q_free, qf_phase, a.timeout_ns)) { failed = 1; break; }
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           mbar_arrive_expect_tx(&q_full, q_bytes);
           for (int c = 0; c < a.n_chunks; ++c)
             tma_load_2d(sQ + c * a.bn * kRowBytes, &tm_q, c * kKAtom,
-                        static_cast<int32_t>(bt * pa.rows_per_batch + nb_ * a.bn), &q_full);
+                        static_cast<int32_t>(static_cast<int64_t>(bt) * pa.rows_per_batch + nb_ * a.bn), &q_full);
           cur_n = n;
         }
         const int s = static_cast<int>(i % kPStages);
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       int64_t cur_n = -1;
       uint32_t q_phase = 0;
       for (int64_t i = 0; i < count && !failed; ++i) {
-        const int64_t t = t0 + i, n = t / pa.m_tiles;
+        const int32_t t = static_cast<int32_t>(t0 + i), n = t / m_tiles32;
         if (n != cur_n) {
           if (cur_n >= 0) mma_commit(&q_free);  // fires when the old tile's MMAs are done
           if (!mbar_wait_bounded(&q_full, q_phase, a.timeout_ns)) { failed = 1; break; }
@@ -331,11 +334,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const int64_t t = t0 + i, n = t / pa.m_tiles, m = t - n * pa.m_tiles;
-      const int64_t bt = n / pa.n_tiles_b, nb_ = n - bt * pa.n_tiles_b;
+      const int32_t t = static_cast<int32_t>(t0 + i), n = t / m_tiles32, m = t - n * m_tiles32;
+      const int32_t bt = n / n_tiles_b32, nb_ = n - bt * n_tiles_b32;
       const int b = static_cast<int>(m) * kTileM + lane_base + lane;
       const bool b_ok = b < a.n_full;
-      float* out = a.scores + bt * pa.scores_per_batch + b;
+      float* out = a.scores + static_cast<int64_t>(bt) * pa.scores_per_batch + b;
       const int q0 = static_cast<int>(nb_) * a.q_per_tile;
       const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc) * a.tmem_cols +
                              (static_cast<uint32_t>(lane_base) << 16);
@@ -559,6 +562,7 @@ PersistPlan persistent_plan(const ScoreProblem& p, const DeviceInfo& dev) {
   pp.bn = choose_bn(pp.m_tiles, nbat * cols_b, dev.sm_count);
   pp.n_tiles_b = (cols_b + pp.bn - 1) / pp.bn;
   pp.tiles = nbat * pp.n_tiles_b * pp.m_tiles;
+  if (pp.tiles > 0x7FFFFFFFLL) return pp;  // the kernel indexes tiles in 32 bits
   const int n_chunks = (p.D + kKAtom - 1) / kKAtom;
   const size_t psmem = static_cast<size_t>(n_chunks) * (pp.bn + kPStages * kTileM) * kRowBytes + 1024;
   pp.ok = pp.bn == 256 && pp.tiles >= 4LL * dev.sm_count &&
