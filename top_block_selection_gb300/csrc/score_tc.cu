@@ -204,6 +204,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int64_t bx = blockIdx.x;
   const int64_t t0 = bx * per + (bx < extra ? bx : extra);
   const int64_t count = per + (blockIdx.x < extra ? 1 : 0);
+  const int32_t count32 = static_cast<int32_t>(count);
   const int32_t m_tiles32 = static_cast<int32_t>(pa.m_tiles);
   const int32_t n_tiles_b32 = static_cast<int32_t>(pa.n_tiles_b);
 
@@ -237,10 +238,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (warp == kPProducerWarp) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      int64_t cur_n = -1, issued = 0;
+      int64_t cur_n = -1;
+      int32_t issued = 0;
       uint32_t qf_phase = 0, q_loads_issued_phase = 0;
       const uint32_t q_bytes = static_cast<uint32_t>(a.n_chunks * a.bn * kRowBytes);
-      for (int64_t i = 0; i < count && !failed; ++i) {
+      for (int32_t i = 0; i < count32 && !failed; ++i) {
         // tile t: column tile g (batch g / n_tiles_b), block tile m
         // 32-bit index arithmetic: the host keeps tiles below 2^31
         const int32_t t = static_cast<int32_t>(t0 + i), n = t / m_tiles32, m = t - n * m_tiles32;
@@ -258,7 +260,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           cur_n = n;
         }
         const int s = static_cast<int>(i % kPStages);
-        const int64_t use = i / kPStages;
+        const int32_t use = i / kPStages;
         if (use > 0 && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((use - 1) & 1), a.timeout_ns)) {
           failed = 1;
           break;
@@ -273,7 +275,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // Loads may still be in flight into shared memory: wait for the last
         // ones issued (bounded) before the CTA may finish.
         atomicOr(a.status, kErrScoreLoadTimeout);
-        for (int64_t j = issued > kPStages ? issued - kPStages : 0; j < issued; ++j)
+        for (int32_t j = issued > kPStages ? issued - kPStages : 0; j < issued; ++j)
           mbar_wait_bounded(&full[j % kPStages], static_cast<uint32_t>((j / kPStages) & 1), a.timeout_ns);
         if (cur_n >= 0) mbar_wait_bounded(&q_full, q_loads_issued_phase, a.timeout_ns);
       }
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const uint32_t idesc = idesc_f16_f32(kTileM, a.bn);
       int64_t cur_n = -1;
       uint32_t q_phase = 0;
-      for (int64_t i = 0; i < count && !failed; ++i) {
+      for (int32_t i = 0; i < count32 && !failed; ++i) {
         const int32_t t = static_cast<int32_t>(t0 + i), n = t / m_tiles32;
         if (n != cur_n) {
           if (cur_n >= 0) mma_commit(&q_free);  // fires when the old tile's MMAs are done
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int half_cols = a.bn >> 1;
     const int c_begin = (warp >> 2) * half_cols;
     constexpr int kQPerLoad = 32 / H;
-    for (int64_t i = 0; i < count; ++i) {
+    for (int32_t i = 0; i < count32; ++i) {
       const int acc = static_cast<int>(i & 1);
       if (failed || !mbar_wait_bounded(&acc_full[acc], static_cast<uint32_t>((i >> 1) & 1), a.timeout_ns)) {
         failed = 1;

@@ -173,7 +173,9 @@ __global__ void __launch_bounds__(kWsWarps * 32)
       // the separate multiply and add do.
       float acc = 0.0f;
       const __half* kb_tail =
-          kb_tail0 + (kb_batch_stride != 0 ? (row / nq_per_batch) * kb_batch_stride : 0);
+          kb_tail0 + (kb_batch_stride != 0
+                          ? static_cast<int64_t>(static_cast<int32_t>(row) / nq_per_batch) * kb_batch_stride
+                          : 0);
       if (lane < H) {
         const __half2* qr = reinterpret_cast<const __half2*>(q16 + (row * H + lane) * D);
         const __half2* kr = reinterpret_cast<const __half2*>(kb_tail);
