@@ -115,10 +115,10 @@ constexpr int kWsMaxNb = 4096;
 constexpr int kWsMinRows = 1024;  // fewer rows: one CTA per row has the lower latency
 
 // Shared bytes of the warp select kernel: per warp, kWarpSelCap candidates
-// and the row's keys (nb rounded up to 4 words).
+// and the staged row (nb + 6 words, rounded up to 4: see the staging).
 inline size_t select_warp_bytes(int32_t nb) {
   return static_cast<size_t>(kWsWarps) *
-         (kWarpSelCap * sizeof(uint64_t) + ((static_cast<size_t>(nb) + 3) & ~static_cast<size_t>(3)) * 4);
+         (kWarpSelCap * sizeof(uint64_t) + ((static_cast<size_t>(nb) + 9) & ~static_cast<size_t>(3)) * 4);
 }
 
 __device__ __forceinline__ void cp_async_4(void* smem_dst, const void* src) {
@@ -145,7 +145,9 @@ __global__ void __launch_bounds__(kWsWarps * 32)
                        int32_t H, int32_t D, int64_t kb_batch_stride, int32_t nq_per_batch) {
   extern __shared__ __align__(16) uint8_t sm_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row_words = (nb + 3) & ~3;
+  // staged positions [0, nb + shift + 3) with shift < 4, rounded up to whole
+  // 16-byte units
+  const int row_words = (nb + 9) & ~3;
   uint64_t* cand = reinterpret_cast<uint64_t*>(sm_raw) + warp * kWarpSelCap;
   float* buf = reinterpret_cast<float*>(sm_raw + kWsWarps * kWarpSelCap * sizeof(uint64_t)) +
                warp * row_words;
@@ -154,17 +156,18 @@ __global__ void __launch_bounds__(kWsWarps * 32)
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWsWarps + warp; row < nq;
        row += static_cast<int64_t>(gridDim.x) * kWsWarps) {
     const float* s = scores_in + row * nb;
+    // Stage the row from the 16-byte units that hold it: element i lands at
+    // buf[i + shift] with shift = (address of s mod 16) / 4, so each unit is
+    // one 16-byte copy (an aligned unit holding a row element never crosses
+    // an allocation granule, so the words beside the row it brings are
+    // readable; they are ignored).
+    const int shift = static_cast<int>((reinterpret_cast<uintptr_t>(s) & 15u) >> 2);
+    const float* s0 = s - shift;
     const int n_copy = kTail ? nb - 1 : nb;
-    if ((reinterpret_cast<uintptr_t>(s) & 15u) == 0 && (n_copy & 3) == 0) {
-      // 16-byte aligned row of whole 16-byte units (every row when nb % 4
-      // == 0 and the scores are 16-byte aligned): a quarter of the copies
-      for (int i = lane * 4; i < n_copy; i += 128)
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(buf + i)),
-                     "l"(reinterpret_cast<uint64_t>(s + i))
-                     : "memory");
-    } else {
-      for (int i = lane; i < n_copy; i += 32) cp_async_4(buf + i, s + i);
-    }
+    for (int p = lane * 4; p < n_copy + shift; p += 128)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(buf + p)),
+                   "l"(reinterpret_cast<uint64_t>(s0 + p))
+                   : "memory");
     asm volatile("cp.async.commit_group;" ::: "memory");
     float tail = 0.0f;
     if constexpr (kTail) {
@@ -199,9 +202,9 @@ __global__ void __launch_bounds__(kWsWarps * 32)
       if (lane == 0) scores_tail[row * nb + (nb - 1)] = tail;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    if (kTail && lane == 0) buf[nb - 1] = tail;
+    if (kTail && lane == 0) buf[nb - 1 + shift] = tail;
     __syncwarp();
-    select_row_warp_f32(buf, nb, k, ids + row * k, cand, lane);
+    select_row_warp_f32(buf, shift, nb, k, ids + row * k, cand, lane);
     __syncwarp();  // the slice is rewritten by the next row
   }
 }

@@ -206,26 +206,41 @@ __device__ __noinline__ void wsel_bisect(const uint32_t* keys, int nb, int kk, u
   wsel_sort_emit<4>(cand, kk, kk, out, lane);
 }
 
-// Exact top-k (k <= 128) of a row of nb fp32 scores in shared memory (16-byte
-// aligned, readable up to nb rounded up to 4) by one warp. The passes compare
-// the scores as floats against the threshold (a float compare orders finite
-// scores as their keys do, -0.0 == +0.0); only candidates are turned into
-// keys, and the bisection fallback first rewrites the row as keys in place.
-// cand: kWarpSelCap 64-bit words of this warp's shared memory. Writes
-// out[0, k).
-__device__ __forceinline__ void select_row_warp_f32(float* row, int nb, int k,
+// The 4 words at buffer positions [p, p + 4) of a staged row (16-byte
+// aligned; p a multiple of 4) whose element i sits at position i + shift;
+// bit j of `valid` is set when element p + j - shift lies in [0, nb).
+__device__ __forceinline__ uint4 wsel_ld4s(const uint32_t* buf, int p, int shift, int nb, uint32_t& valid) {
+  const uint4 v = *reinterpret_cast<const uint4*>(buf + p);
+  const int lo = shift - p, hi = nb + shift - p;  // valid j: lo <= j < hi
+  valid = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) valid |= (j >= lo && j < hi ? 1u : 0u) << j;
+  return v;
+}
+
+// Exact top-k (k <= 128) of a row of nb fp32 scores staged in shared memory
+// by one warp: element i at buf[i + shift] (0 <= shift < 4, buf 16-byte
+// aligned and readable up to nb + shift rounded up to 4; the other words
+// there may hold anything). The passes compare the scores as floats against
+// the threshold (a float compare orders finite scores as their keys do, -0.0
+// == +0.0); only candidates are turned into keys; the bisection fallback
+// first moves the row to shift 0 and rewrites it as keys in place. The 128
+// segments of the threshold are the buffer positions mod 128. cand:
+// kWarpSelCap 64-bit words of this warp's shared memory. Writes out[0, k).
+__device__ __forceinline__ void select_row_warp_f32(float* buf, int shift, int nb, int k,
                                                     int32_t* __restrict__ out, uint64_t* cand, int lane) {
   const int kk = k < nb ? k : nb;
   for (int j = kk + lane; j < k; j += 32) out[j] = -1;
   if (kk <= 0) return;
-  const uint32_t* rowu = reinterpret_cast<const uint32_t*>(row);
+  const uint32_t* bufu = reinterpret_cast<const uint32_t*>(buf);
+  const int end = nb + shift;  // buffer positions in use
   float tf = -__int_as_float(0x7f800000);  // -inf: every finite score is a candidate
   uint32_t T = 0, mx = 0;
   if (kk < nb) {
-    float m[4] = {tf, tf, tf, tf};  // segment 4 lane + j of {index mod 128}
-    for (int base = lane * 4; base < nb; base += 128) {
+    float m[4] = {tf, tf, tf, tf};  // segment 4 lane + j of {position mod 128}
+    for (int p = lane * 4; p < end; p += 128) {
       uint32_t valid;
-      const uint4 v = wsel_ld4(rowu, base, nb, valid);
+      const uint4 v = wsel_ld4s(bufu, p, shift, nb, valid);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         if ((valid >> j) & 1u) m[j] = fmaxf(m[j], __uint_as_float(wsel_get(v, j)));
@@ -241,9 +256,9 @@ __device__ __forceinline__ void select_row_warp_f32(float* row, int nb, int k,
     tf = key_to_score(T);
   }
   uint32_t c = 0;
-  for (int base = lane * 4; base < nb; base += 128) {
+  for (int p = lane * 4; p < end; p += 128) {
     uint32_t valid;
-    const uint4 v = wsel_ld4(rowu, base, nb, valid);
+    const uint4 v = wsel_ld4s(bufu, p, shift, nb, valid);
 #pragma unroll
     for (int j = 0; j < 4; ++j) c += ((valid >> j) & 1u) && __uint_as_float(wsel_get(v, j)) >= tf ? 1u : 0u;
   }
@@ -251,13 +266,13 @@ __device__ __forceinline__ void select_row_warp_f32(float* row, int nb, int k,
   const uint32_t n_c = __shfl_sync(0xFFFFFFFFu, incl, 31);
   if (n_c <= static_cast<uint32_t>(kWarpSelCap)) {
     uint32_t o = incl - c;
-    for (int base = lane * 4; base < nb; base += 128) {
+    for (int p = lane * 4; p < end; p += 128) {
       uint32_t valid;
-      const uint4 v = wsel_ld4(rowu, base, nb, valid);
+      const uint4 v = wsel_ld4s(bufu, p, shift, nb, valid);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float x = __uint_as_float(wsel_get(v, j));
-        if (((valid >> j) & 1u) && x >= tf) cand[o++] = win_key(score_key(x), base + j);
+        if (((valid >> j) & 1u) && x >= tf) cand[o++] = win_key(score_key(x), p + j - shift);
       }
     }
     __syncwarp();
@@ -265,10 +280,18 @@ __device__ __forceinline__ void select_row_warp_f32(float* row, int nb, int k,
     else wsel_sort_emit<8>(cand, static_cast<int>(n_c), kk, out, lane);
     return;
   }
-  // Flat or tied rows (kk < nb here): the row as keys, then the bisection.
-  uint32_t* keys = reinterpret_cast<uint32_t*>(row);
-  for (int i = lane; i < nb; i += 32) keys[i] = score_key(row[i]);
-  __syncwarp();
+  // Flat or tied rows (kk < nb here): the row moved to shift 0 (chunks of 32
+  // in increasing order: each chunk's words are read before they are
+  // overwritten, and a write never lands on a word still to be read), then
+  // rewritten as keys, then the bisection.
+  uint32_t* keys = reinterpret_cast<uint32_t*>(buf);
+  for (int i0 = 0; i0 < nb; i0 += 32) {
+    const int i = i0 + lane;
+    const float x = i < nb ? buf[i + shift] : 0.0f;
+    __syncwarp();
+    if (i < nb) keys[i] = score_key(x);
+    __syncwarp();
+  }
   wsel_bisect(keys, nb, kk, T, mx, out, cand, lane);
 }
 
