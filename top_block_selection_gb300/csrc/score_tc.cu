@@ -192,9 +192,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   const int a_bytes = a.n_chunks * kTileM * kRowBytes;  // one kb stage
-  uint8_t* sQ = smem;                                    // n_chunks x [bn rows x 128 B]
-  uint8_t* sA = sQ + a.n_chunks * a.bn * kRowBytes;      // kPStages kb stages
-  __shared__ uint64_t full[kPStages], empty[kPStages], acc_full[2], acc_empty[2], q_full, q_free;
+  const int q_tile_bytes = a.n_chunks * a.bn * kRowBytes;
+  uint8_t* sQbase = smem;                                // 2 x n_chunks x [bn rows x 128 B]
+  uint8_t* sA = sQbase + 2 * q_tile_bytes;               // kPStages kb stages
+  // Two query-tile buffers: the j-th query tile of the run goes to buffer
+  // j % 2, loaded as soon as the MMAs on tile j - 2 are done, so a change of
+  // query tile does not wait for its load.
+  __shared__ uint64_t full[kPStages], empty[kPStages], acc_full[2], acc_empty[2], q_full[2], q_free[2];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int failed;
 
@@ -218,8 +222,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(&acc_full[s], 1);
       mbar_init(&acc_empty[s], 32 * kPEpiWarps);
     }
-    mbar_init(&q_full, 1);
-    mbar_init(&q_free, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_free[s], 1);
+    }
     failed = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tm_kb);
@@ -240,23 +246,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) {
       int64_t cur_n = -1;
       int32_t issued = 0;
-      uint32_t qf_phase = 0, q_loads_issued_phase = 0;
-      const uint32_t q_bytes = static_cast<uint32_t>(a.n_chunks * a.bn * kRowBytes);
+      int32_t jq = -1;  // query tiles of the run loaded so far, minus one
+      const uint32_t q_bytes = static_cast<uint32_t>(q_tile_bytes);
       for (int32_t i = 0; i < count32 && !failed; ++i) {
         // tile t: column tile g (batch g / n_tiles_b), block tile m
         // 32-bit index arithmetic: the host keeps tiles below 2^31
         const int32_t t = static_cast<int32_t>(t0 + i), n = t / m_tiles32, m = t - n * m_tiles32;
         const int32_t bt = n / n_tiles_b32, nb_ = n - bt * n_tiles_b32;
         if (n != cur_n) {
-          if (cur_n >= 0) {  // every MMA on the previous query tile has completed
-            if (!mbar_wait_bounded(&q_free, qf_phase, a.timeout_ns)) { failed = 1; break; }
-            qf_phase ^= 1u;
+          ++jq;
+          const int qb = jq & 1;
+          // buffer qb is free once every MMA on query tile jq - 2 has completed
+          if (jq >= 2 && !mbar_wait_bounded(&q_free[qb], static_cast<uint32_t>(((jq >> 1) - 1) & 1),
+                                            a.timeout_ns)) {
+            failed = 1;
+            break;
           }
-          if (cur_n >= 0) q_loads_issued_phase ^= 1u;  // phase of the load issued now
-          mbar_arrive_expect_tx(&q_full, q_bytes);
+          mbar_arrive_expect_tx(&q_full[qb], q_bytes);
           for (int c = 0; c < a.n_chunks; ++c)
-            tma_load_2d(sQ + c * a.bn * kRowBytes, &tm_q, c * kKAtom,
-                        static_cast<int32_t>(static_cast<int64_t>(bt) * pa.rows_per_batch + nb_ * a.bn), &q_full);
+            tma_load_2d(sQbase + qb * q_tile_bytes + c * a.bn * kRowBytes, &tm_q, c * kKAtom,
+                        static_cast<int32_t>(static_cast<int64_t>(bt) * pa.rows_per_batch + nb_ * a.bn),
+                        &q_full[qb]);
           cur_n = n;
         }
         const int s = static_cast<int>(i % kPStages);
@@ -277,7 +287,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         atomicOr(a.status, kErrScoreLoadTimeout);
         for (int32_t j = issued > kPStages ? issued - kPStages : 0; j < issued; ++j)
           mbar_wait_bounded(&full[j % kPStages], static_cast<uint32_t>((j / kPStages) & 1), a.timeout_ns);
-        if (cur_n >= 0) mbar_wait_bounded(&q_full, q_loads_issued_phase, a.timeout_ns);
+        for (int32_t j = jq > 1 ? jq - 1 : 0; j <= jq; ++j)  // the (up to) two query loads in flight
+          mbar_wait_bounded(&q_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), a.timeout_ns);
       }
     }
   } else if (warp == kPMmaWarp) {
@@ -285,15 +296,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_f16_f32(kTileM, a.bn);
       int64_t cur_n = -1;
-      uint32_t q_phase = 0;
+      int32_t jq = -1;  // the run's query tile in use
       for (int32_t i = 0; i < count32 && !failed; ++i) {
         const int32_t t = static_cast<int32_t>(t0 + i), n = t / m_tiles32;
         if (n != cur_n) {
-          if (cur_n >= 0) mma_commit(&q_free);  // fires when the old tile's MMAs are done
-          if (!mbar_wait_bounded(&q_full, q_phase, a.timeout_ns)) { failed = 1; break; }
-          q_phase ^= 1u;
+          if (jq >= 0) mma_commit(&q_free[jq & 1]);  // fires when the old tile's MMAs are done
+          ++jq;
+          if (!mbar_wait_bounded(&q_full[jq & 1], static_cast<uint32_t>((jq >> 1) & 1), a.timeout_ns)) {
+            failed = 1;
+            break;
+          }
           cur_n = n;
         }
+        uint8_t* sQ = sQbase + (jq & 1) * q_tile_bytes;
         const int s = static_cast<int>(i % kPStages);
         const int acc = static_cast<int>(i & 1);
         if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((i / kPStages) & 1), a.timeout_ns)) {
@@ -566,7 +581,7 @@ PersistPlan persistent_plan(const ScoreProblem& p, const DeviceInfo& dev) {
   pp.tiles = nbat * pp.n_tiles_b * pp.m_tiles;
   if (pp.tiles > 0x7FFFFFFFLL) return pp;  // the kernel indexes tiles in 32 bits
   const int n_chunks = (p.D + kKAtom - 1) / kKAtom;
-  const size_t psmem = static_cast<size_t>(n_chunks) * (pp.bn + kPStages * kTileM) * kRowBytes + 1024;
+  const size_t psmem = static_cast<size_t>(n_chunks) * (2 * pp.bn + kPStages * kTileM) * kRowBytes + 1024;
   pp.ok = pp.bn == 256 && pp.tiles >= 4LL * dev.sm_count &&
           psmem <= static_cast<size_t>(dev.max_smem_optin) - 1024;
   return pp;
@@ -604,7 +619,7 @@ cudaError_t launch_scores(const ScoreProblem& p, const DeviceInfo& dev, cudaStre
     a.kb_z = p.kb_batch_stride != 0 ? 1 : 0;
     // Many full-width tiles: the persistent kernel (one CTA per SM, pipelined
     // loads, MMAs and epilogue); the same arithmetic per score.
-    const size_t psmem = static_cast<size_t>(a.n_chunks) * (bn + kPStages * kTileM) * kRowBytes + 1024;
+    const size_t psmem = static_cast<size_t>(a.n_chunks) * (2 * bn + kPStages * kTileM) * kRowBytes + 1024;
     if (pp.ok) {
       const uint64_t zs = p.kb_batch_stride != 0 ? static_cast<uint64_t>(nbat) : 1u;
       const uint64_t zst = p.kb_batch_stride != 0 ? static_cast<uint64_t>(p.kb_batch_stride)
