@@ -115,6 +115,46 @@ __device__ __forceinline__ void split_rank(const uint64_t* x, int n, int gtid, E
   }
 }
 
+// The same ranks over pairs: x is 16-byte aligned and, for odd n, x[n] == 0
+// (below every winner key). Thread slot (pair e, sub) compares both elements
+// of pair e against the pairs sub, sub + P, ... (one 16-byte load for two
+// elements), so a comparison costs half the shared-memory loads of
+// split_rank; P is the largest power of two <= 32 with 2 P ceil(n / 2) <= T
+// (at least 1).
+template <int T, typename Emit>
+__device__ __forceinline__ void pair_rank(const uint64_t* x, int n, int gtid, Emit emit) {
+  const int np = (n + 1) >> 1;
+  int P = 1;
+  while (P < 32 && 2 * P * np <= T) P <<= 1;
+  const int slots = np * P;
+  const ulonglong2* x2 = reinterpret_cast<const ulonglong2*>(x);
+  for (int base = 0; base < slots; base += T) {
+    const int t = base + gtid;
+    const int e = t / P;
+    const int sub = t & (P - 1);
+    const bool valid = t < slots;
+    ulonglong2 me = make_ulonglong2(0ull, 0ull);
+    uint32_t r0 = 0, r1 = 0;
+    if (valid) {
+      me = x2[e];
+#pragma unroll 4
+      for (int m = sub; m < np; m += P) {
+        const ulonglong2 v = x2[m];
+        r0 += (v.x > me.x ? 1u : 0u) + (v.y > me.x ? 1u : 0u);
+        r1 += (v.x > me.y ? 1u : 0u) + (v.y > me.y ? 1u : 0u);
+      }
+    }
+    for (int o = 1; o < P; o <<= 1) {
+      r0 += __shfl_xor_sync(0xFFFFFFFFu, r0, o);
+      r1 += __shfl_xor_sync(0xFFFFFFFFu, r1, o);
+    }
+    if (valid && sub == 0) {
+      emit(2 * e, r0);
+      if (2 * e + 1 < n) emit(2 * e + 1, r1);
+    }
+  }
+}
+
 // Finds the digit of the bins [0, NBINS) holding the need-th largest key
 // (counting from the top bin down); writes digit, count above it and its own
 // count to sh. Thread t owns the B = NBINS / T bins [NBINS - (t+1)B, NBINS -
@@ -513,25 +553,30 @@ __device__ bool select_row_window(const uint32_t (&key)[R], int nb, int k,
 //     a warp max with the round's maxima removed (equal maxima leave together,
 //     which can only lower t_w). At least q keys of warp w are >= t_w, so at
 //     least k keys of the row are >= T = min_w t_w: every winner is >= T.
-//   * the keys >= T (about 1.5-2 k on score rows) are gathered by a warp scan
-//     and one shared counter per warp, and each is ranked among them by
-//     (key, index) (split_rank); ranks below k are the output slots.
-// Two group barriers in all. Returns false, after a barrier and having
+//   * the keys >= T (about 1.5-2 k on score rows) are gathered in thread
+//     order (a warp scan, then the warps' totals), and each is ranked among
+//     them by (key, index) (pair_rank); ranks below k are the output slots.
+// Three group barriers in all. Returns false, after a barrier and having
 // written nothing but cand and sh, when more than kSelBinMax keys are >= T
 // (ties or flat rows), or when k >= nb or k > kSelThrKMax; the caller then
-// runs the window select (hist must still be zero for it).
+// runs the window select (hist must still be zero for it). cand must be
+// 16-byte aligned.
 // Measured against the window select on the same rows (one 256-thread CTA
 // per row, three per SM): 3,856 vs 4,297 cycles per 2048-key row, 2,646 vs
-// 3,800 per 513-key row. Gathering into per-warp slots without the shared
-// counter, or ranking with warp sums, or sorting the candidates with one
-// warp's bitonic network were each slower (4,365 / 5,557 cycles): shuffles
-// and warp reductions are the scarce resource when several CTAs share an SM.
+// 3,800 per 513-key row. Gathering into per-warp slots, or ranking with warp
+// sums, or sorting the candidates with one warp's bitonic network were each
+// slower (4,365 / 5,557 cycles): shuffles and warp reductions are the scarce
+// resource when several CTAs share an SM. The gather by the warps' totals
+// instead of one shared counter, and the ranking over pairs instead of
+// single elements, took a 2048-key row from 3,314 to 3,126 cycles (one CTA
+// per SM) and from 4,038 to 3,795 (one CTA per row).
 constexpr int kSelThrKMax = 128;
 
 template <int T, int R>
 __device__ bool select_row_thr(const uint32_t (&key)[R], int nb, int k, int32_t* __restrict__ out,
                                uint64_t* cand, SelectShared& sh, int gtid, int bar_id) {
   constexpr int kWarps = T / 32;
+  static_assert(2 * kWarps <= 32, "sh.wsum holds the warps' thresholds and totals");
   if (k >= nb || k > kSelThrKMax) return false;
   const int lane = gtid & 31, warp = gtid >> 5;
   const int q = (k + kWarps - 1) / kWarps;
@@ -544,7 +589,6 @@ __device__ bool select_row_thr(const uint32_t (&key)[R], int nb, int k, int32_t*
     if (v == t) v = 0;
   }
   if (lane == 0) sh.wsum[warp] = t;
-  if (gtid == 0) sh.n_cand = 0;
   group_sync<T>(bar_id);
   uint32_t thr = 0xFFFFFFFFu;
 #pragma unroll
@@ -558,10 +602,15 @@ __device__ bool select_row_thr(const uint32_t (&key)[R], int nb, int k, int32_t*
     const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, off);
     if (lane >= off) incl += x;
   }
-  uint32_t base = 0;
-  if (lane == 31) base = atomicAdd(&sh.n_cand, incl);
-  base = __shfl_sync(0xFFFFFFFFu, base, 31);
-  uint32_t o = base + incl - c;
+  if (lane == 31) sh.wsum[kWarps + warp] = incl;
+  group_sync<T>(bar_id);
+  uint32_t o = incl - c, n_c = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t x = sh.wsum[kWarps + w];
+    o += w < warp ? x : 0u;
+    n_c += x;
+  }
 #pragma unroll
   for (int j = 0; j < R; ++j) {
     if (j * T + gtid < nb && key[j] >= thr) {
@@ -569,13 +618,14 @@ __device__ bool select_row_thr(const uint32_t (&key)[R], int nb, int k, int32_t*
       ++o;
     }
   }
+  // pair_rank reads cand[n_c] for odd n_c: a zero key ranks below them all.
+  if (gtid == 0 && (n_c & 1u) && n_c < static_cast<uint32_t>(kSelBinMax)) cand[n_c] = 0ull;
   group_sync<T>(bar_id);
-  const uint32_t n_c = sh.n_cand;
   if (n_c > static_cast<uint32_t>(kSelBinMax)) {
-    group_sync<T>(bar_id);  // every thread has read n_cand before sh is reused
+    group_sync<T>(bar_id);  // every thread is past its reads of sh before it is reused
     return false;
   }
-  split_rank<T>(cand, static_cast<int>(n_c), gtid, [&](int e, uint32_t r) {
+  pair_rank<T>(cand, static_cast<int>(n_c), gtid, [&](int e, uint32_t r) {
     if (r < static_cast<uint32_t>(k)) out[r] = static_cast<int32_t>(~static_cast<uint32_t>(cand[e]));
   });
   return true;
