@@ -426,6 +426,45 @@ def test_select_exact_many_rows(tbs, kind, nb, k):
     assert np.array_equal(ids.cpu().numpy(), orc.select_topk(s, k))
 
 
+def _threshold_rows(k, extras, nb=1024, threads=256):
+    """Score rows that steer the CTA-per-row threshold select to a chosen
+    number of candidates. Thread t of the 256-thread select holds the keys of
+    indices t + 256 j; warp w = t // 32 takes the ceil(k/8)-th largest of its
+    threads' maxima. Each warp gets exactly ceil(k/8) threads with a high
+    maximum (>= 100, except one of warp 0's at 10.0), so the bound is 10.0 and
+    the keys >= it are those 8 ceil(k/8) maxima plus `extras` further keys in
+    (10, 99) placed in the high threads' other slots; every other key is below
+    1. All values are distinct. The oracle decides the expected ids, so a row
+    stays a valid exactness case whatever path the kernel takes."""
+    q = -(-k // 8)
+    rng = np.random.default_rng(1000 * k + extras)
+    row = (rng.permutation(nb).astype(np.float64) * 1e-4).astype(np.float32)
+    slots = []
+    for w in range(threads // 32):
+        for i in range(q):
+            t = 32 * w + i
+            row[t] = 10.0 if (w == 0 and i == q - 1) else np.float32(100.0 + 0.01 * t)
+            if not (w == 0 and i == q - 1):
+                slots += [t + threads * j for j in range(1, nb // threads)]
+    assert extras <= len(slots)
+    for e, idx in enumerate(rng.permutation(slots)[:extras]):
+        row[idx] = np.float32(11.0 + 0.01 * e)
+    return row
+
+
+@pytest.mark.parametrize("k,extras", [(64, 0), (64, 1), (64, 3), (64, 189), (128, 1), (128, 127),
+                                      (128, 128), (128, 129)])
+def test_select_threshold_candidate_counts(tbs, k, extras):
+    """The threshold select around its limits: an odd number of candidates
+    (the ranking reads one padding entry past them), exactly 255 and 256
+    candidates (the most it ranks) and 257 (more: the window select takes the
+    row)."""
+    rows = np.stack([_threshold_rows(k, extras), _threshold_rows(k, extras)[::-1].copy()])
+    ids = tbs.qsa_select(dev(rows), k)
+    torch.cuda.synchronize()
+    assert np.array_equal(ids.cpu().numpy(), orc.select_topk(rows, k))
+
+
 def test_select_empty_rows(tbs):
     ids = tbs.qsa_select(torch.zeros((4, 0), dtype=torch.float32, device="cuda"), 3)
     torch.cuda.synchronize()
