@@ -76,6 +76,19 @@ def test_decode_shapes(tbs, w):
     assert np.array_equal(ids_gpu.cpu().numpy(), orc.select_topk(s, w.k))
 
 
+@pytest.mark.parametrize("tied", [False, True])
+@pytest.mark.parametrize("nb,k", [(2, 1), (32, 31), (33, 33), (64, 8), (64, 67)])
+def test_short_rows_one_warp_select(tbs, nb, k, tied):
+    """Rows of at most 64 blocks take the one-warp select in the fused step:
+    ids exact against the oracle on the GPU's scores, including k >= nb (ids
+    past nb are -1) and rows whose full blocks all tie (the block-index
+    tie-break)."""
+    q, kb = qi.random_case(40, 8, 128, nb, seed=nb * 13 + k, scale=0.3)
+    if tied:
+        kb[:] = kb[0]
+    check_case(tbs, q, kb, nb * 64 - 5, 64, k, f"short-{nb}-{k}-{tied}")
+
+
 @pytest.mark.parametrize("H", [1, 2, 4, 8, 16, 32])
 @pytest.mark.parametrize("D", [16, 64, 80, 128, 256])
 def test_coordinate_coded_exact(tbs, H, D):
@@ -402,8 +415,8 @@ def test_determinism_double_launch(tbs):
 
 
 @pytest.mark.parametrize("kind", ["normal", "ties", "signed0", "const"])
-@pytest.mark.parametrize("nb,k", [(1, 1), (5, 8), (33, 8), (100, 64), (1000, 100), (2049, 64),
-                                  (4096, 1024), (32768, 64), (300, 300)])
+@pytest.mark.parametrize("nb,k", [(1, 1), (5, 8), (33, 8), (64, 63), (64, 70), (65, 8), (100, 64),
+                                  (1000, 100), (2049, 64), (4096, 1024), (32768, 64), (300, 300)])
 def test_select_exact(tbs, kind, nb, k):
     nq = 3 if nb >= 4096 else 23
     s = qi.random_scores(nq, nb, seed=nb * 31 + k, kind=kind)

@@ -598,7 +598,21 @@ __global__ void __maxnreg__(kForm == kFormLean ? 72 : 96)
     int32_t* out = idsb + static_cast<int64_t>(qi) * a.k;
     const float* row = scoresb + static_cast<int64_t>(qi) * a.nb;
     const uint32_t* rk = reinterpret_cast<const uint32_t*>(smem + a.rows_off + r * a.row_bytes);
-    if (a.nb <= 8 * kWork) {
+    if (a.nb <= 64) {
+      // Short rows: one warp, no block barrier (the other warps go on to the
+      // loop's barrier).
+      if (warp == 0) {
+        uint32_t k0 = 0, k1 = 0;
+        if (a.dsmem) {
+          if (lane < a.nb) k0 = rk[lane];
+          if (lane + 32 < a.nb) k1 = rk[lane + 32];
+        } else {
+          if (lane < a.nb) k0 = score_key(__ldcg(row + lane));
+          if (lane + 32 < a.nb) k1 = score_key(__ldcg(row + lane + 32));
+        }
+        select_row_warp64(k0, k1, a.nb, a.k, out, lane);
+      }
+    } else if (a.nb <= 8 * kWork) {
       uint32_t key[8];
       if (a.dsmem) load_keys_regs<kWork, 8>(rk, a.nb, key, hist, tid);
       else load_keys_regs_global<kWork, 8>(row, a.nb, key, hist, tid);

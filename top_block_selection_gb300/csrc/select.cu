@@ -97,6 +97,15 @@ __global__ void __launch_bounds__(kWinThreads, 3)
   const int64_t row = blockIdx.x;
   pdl_launch_dependents();
   pdl_wait();  // the scores may come from the previous kernel on the stream
+  if (nb <= 64) {  // short rows: one warp, no block barrier
+    if (tid < 32) {
+      const float* s = scores + row * nb;
+      const uint32_t k0 = tid < nb ? score_key(__ldcg(s + tid)) : 0u;
+      const uint32_t k1 = tid + 32 < nb ? score_key(__ldcg(s + tid + 32)) : 0u;
+      select_row_warp64(k0, k1, nb, k, ids + row * k, tid);
+    }
+    return;
+  }
   uint32_t key[R];
   load_keys_regs_global<kWinThreads, R>(scores + row * nb, nb, key, hist, tid);
   int32_t* out = ids + row * k;

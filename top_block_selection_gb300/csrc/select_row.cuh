@@ -545,6 +545,31 @@ __device__ bool select_row_window(const uint32_t (&key)[R], int nb, int k,
   return true;
 }
 
+// ------------------------------------------ one warp, rows of <= 64 keys
+// Short rows (nb <= 64): lane l holds the keys of indices l and l + 32 (any
+// value past nb: those entries never count), and every key is ranked against
+// the others by (key, index) with shuffles; ranks below k are the output
+// slots and slots past nb get -1. No block barrier: the rest of the group
+// may idle.
+__device__ __forceinline__ void select_row_warp64(uint32_t key0, uint32_t key1, int nb, int k,
+                                                  int32_t* __restrict__ out, int lane) {
+  const bool v0 = lane < nb, v1 = lane + 32 < nb;
+  // A winner key is never 0 (its low word is ~index), so 0 marks an empty entry.
+  const uint64_t w0 = v0 ? win_key(key0, lane) : 0ull;
+  const uint64_t w1 = v1 ? win_key(key1, lane + 32) : 0ull;
+  uint32_t r0 = 0, r1 = 0;
+#pragma unroll 8
+  for (int s = 0; s < 32; ++s) {
+    const uint64_t y0 = __shfl_sync(0xFFFFFFFFu, w0, s);
+    const uint64_t y1 = __shfl_sync(0xFFFFFFFFu, w1, s);
+    r0 += (y0 > w0 ? 1u : 0u) + (y1 > w0 ? 1u : 0u);
+    r1 += (y0 > w1 ? 1u : 0u) + (y1 > w1 ? 1u : 0u);
+  }
+  if (v0 && r0 < static_cast<uint32_t>(k)) out[r0] = lane;
+  if (v1 && r1 < static_cast<uint32_t>(k)) out[r1] = lane + 32;
+  for (int j = nb + lane; j < k; j += 32) out[j] = -1;
+}
+
 // ------------------------------------------- threshold select (registers)
 // For k <= kSelThrKMax and k < nb: a lower bound T of the k-th largest key
 // from per-thread maxima, then an exact rank of the few keys >= T.
