@@ -46,9 +46,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # sources have changed since reports null. The captures and their commands
 # are summarised in profiles/.
 NCU_TRAFFIC = {
-    "fused_step_kernel": {"bytes_per_launch": 1646592,
+    "fused_step_kernel": {"bytes_per_launch": 1651200,
                           "sources": ["fused_kernel.cuh", "select_row.cuh", "qsa_device.cuh"],
-                          "source_sha": "f91ddd06733fed1a",
+                          "source_sha": "0f670db82810e77e",
                           "workload": "long128k_nq256_h8_d128_kv131072"},
     "split_cluster_kernel": {"bytes_per_launch": 17340544,
                              "sources": ["split_reduce.cu", "qsa_device.cuh", "qsa_internal.h"],

@@ -3,9 +3,9 @@
 // over the block scores, here with a block-index tie-break).
 //
 // Rows of up to 4096 blocks: one CTA of 8 warps per row, the row's keys in
-// registers, the selects of the fused kernel (select_row_thr for k <= 128 on
-// rows of up to 1024 blocks, then select_row_window, with select_row_regs
-// behind it). Longer rows: a CTA of kSelThreads threads
+// registers, the selects of the fused kernel (select_row_warp64 by one warp
+// on rows of at most 64 blocks; select_row_thr for k <= 128 on rows of up to
+// 1024 blocks, then select_row_window, with select_row_regs behind it). Longer rows: a CTA of kSelThreads threads
 // selects several rows, kSelG warps per row (select_row_g): the row's keys
 // are staged in shared memory, the first 11-bit radix digit finds the
 // boundary bin, the boundary bin's keys are compacted and refined, and the

@@ -6,7 +6,8 @@
 // tie-break): descending score; equal scores -> smaller block index first;
 // -0.0 == +0.0; ids past nb are -1.
 //
-// Scores are compared as order-preserving uint32 keys (score_key). For k <=
+// Scores are compared as order-preserving uint32 keys (score_key). Rows of
+// at most 64 keys are ranked by one warp (select_row_warp64). For k <=
 // 128, register-held rows first try a threshold select (select_row_thr: a
 // lower bound of the k-th key from per-thread maxima, then an exact rank of
 // the few keys above it). Otherwise the search is a radix select on the keys,
