@@ -42,9 +42,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic per launch from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by kernel, with the SHA-256 (first 16 hex
-# digits) of the kernel's source files at capture time; an entry whose
-# sources have changed since reports null. The captures and their commands
-# are summarised in profiles/.
+# digits) of the kernel's source files at capture time, or after a later edit
+# that leaves the kernel's device code as captured (comments; host-side
+# declarations in a shared header); an entry whose sources have changed
+# otherwise reports null. The captures and their commands are summarised in
+# profiles/.
 NCU_TRAFFIC = {
     "fused_step_kernel": {"bytes_per_launch": 1651200,
                           "sources": ["fused_kernel.cuh", "select_row.cuh", "qsa_device.cuh"],
@@ -52,7 +54,7 @@ NCU_TRAFFIC = {
                           "workload": "long128k_nq256_h8_d128_kv131072"},
     "split_cluster_kernel": {"bytes_per_launch": 17340544,
                              "sources": ["split_reduce.cu", "qsa_device.cuh", "qsa_internal.h"],
-                             "source_sha": "be685f81be541f5b",
+                             "source_sha": "d789cc2cc8faa7dc",
                              "workload": "split_g4_r8_c128_b2048"},
 }
 
