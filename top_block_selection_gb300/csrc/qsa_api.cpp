@@ -186,7 +186,8 @@ const char* qsa_arm(void) {
   int n = snprintf(buf, sizeof buf,
                    "sm_103a: TMA + tcgen05.mma kind::f16 (M128, fp32 in TMEM) scorer with fused "
                    "ReLU/head-sum epilogue; fp32 pinned-order tail (+1e9); exact top-k select "
-                   "(threshold + rank for k <= 128, radix select otherwise; "
+                   "(one warp for rows of <= 64 blocks, threshold + rank for k <= 128, radix "
+                   "select otherwise; "
                    "block-index tie-break); cvt.rn fp32->fp16 stage | last call on this thread: ");
   if (!t_plan_any) {
     snprintf(buf + n, sizeof buf - n, "none");
